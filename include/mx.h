@@ -1,0 +1,164 @@
+/*
+ * mx.h - C ABI of libmx: low-batch MXFP8 block-scaled projections on GB300 (sm_103a).
+ *
+ * MXFP8 here means: E4M3 (fn) values with one UE8M0 power-of-two scale per 32
+ * consecutive elements along K (sf_vec_size 32), as the vLLM page
+ * "vllm.models.deepseek_v41.nvidia.specialized_decode.attention.mxfp8"
+ * describes for fused_wqa_wkv, wq_b and wo_b (module docstring;
+ * `compile_low_latency`: Float8E4M3FN operands, Float8E8M0FNU scales, bf16 out).
+ *
+ * Conventions shared by every entry point:
+ *  - Every data pointer is a DEVICE pointer owned by the caller. No call
+ *    allocates or frees memory; the handle owns only a 4-byte status word.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream) and must be made with the handle's
+ *    device current.
+ *  - Arguments are validated before anything is launched: on any error the
+ *    outputs are left untouched and nothing is enqueued (the page
+ *    "vllm.models.deepseek_v41.nvidia.ops.cute_dsl", `_consumer`: a bad
+ *    argument raises before the call's first launch).
+ *  - Activation scales and weight scales use the F8_128x4 swizzled layout:
+ *    the [rows, K/32] scale matrix is padded to ceil128(rows) x ceil4(K/32)
+ *    and cut into 128x4 tiles of 512 contiguous bytes (tiles row-major); inside
+ *    a tile, (r, c) sits at byte 16*(r%32) + 4*(r/32) + c. Buffer size:
+ *    mx_scale_bytes(rows, K).
+ *  - Weights are [N, K] row-major E4M3 (K contiguous), i.e. the column-major
+ *    [K, N] weight of `launch_low_latency`.
+ */
+#ifndef MX_H_
+#define MX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1, /* null/misaligned pointer, size out of range        */
+  MX_ERR_UNSUPPORTED = 2, /* shape outside what the kernels take: caller falls
+                             back (the page's functions return None there)    */
+  MX_ERR_DEVICE = 3,      /* not a compute-capability 10.3 device, or a call
+                             made with another device current                 */
+  MX_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed             */
+  MX_ERR_TIMEOUT = 5      /* a bounded device-side wait expired (see
+                             mx_device_status)                                 */
+};
+
+/* Flags for mx_gemm. */
+#define MX_FLAG_PDL 1u /* launch with programmatic stream serialization: the
+                          kernel streams its weights before waiting for the
+                          previous kernel on the stream (`launch_low_latency`
+                          / module docstring of the mxfp8 page)              */
+
+typedef struct mx_handle mx_handle;
+
+/* Weight operand of one projection: E4M3 [n, k] plus swizzled scales. */
+typedef struct mx_weight {
+  const void* w;        /* [n, k] E4M3, 16-byte aligned                      */
+  const void* w_scales; /* mx_scale_bytes(n, k) bytes, 32-byte aligned       */
+  int n;                /* output features, multiple of 128                  */
+  int k;                /* input features, multiple of 128                   */
+} mx_weight;
+
+/* Create a handle for `device`. Checks compute capability 10.3 (the device
+ * gate of `_cute_dsl_runner` / `_wide_supported` on the mxfp8 page), loads the
+ * kernels and allocates the 4-byte device status word.
+ * Returns MX_ERR_DEVICE on another architecture, MX_ERR_CUDA if no device. */
+int mx_create(mx_handle** h, int device);
+int mx_destroy(mx_handle* h);
+
+/* Bytes of a swizzled scale buffer for a [rows, k] MXFP8 operand:
+ * ceil128(rows) * ceil4(k/32) (`mxfp8_scale_bytes` on the mxfp8 page, `_zeros`).
+ * Returns 0 for rows < 0 or k not a multiple of 32. */
+size_t mx_scale_bytes(int rows, int k);
+
+/* Quantize bf16 rows to MXFP8 (the role of `mxfp8_e4m3_quantize(a,
+ * is_sf_swizzled_layout=True)` in `wide_mm` / `pinned_mm` on the mxfp8 page).
+ *   x      [M, K] bf16, row stride ldx elements (ldx >= K, ldx % 8 == 0),
+ *          16-byte aligned.
+ *   q      [M, K] E4M3 out, row stride K, 16-byte aligned.
+ *   scales out: swizzled (mx_scale_bytes(M, K) bytes, padding written as 0)
+ *          when swizzled != 0, else plain row-major [M, K/32].
+ * Per 32-block: e = floor(log2 amax) - 8 clamped to [-127, 127] (e = -127
+ * for a zero block), codes = E4M3 saturating round-to-nearest-even of
+ * x * 2^-e, scale byte e + 127; a block holding NaN/Inf gets scale 0xFF and
+ * NaN codes. Constraints: 1 <= M <= 65536, K % 32 == 0, K > 0. */
+int mx_quantize_rows(mx_handle* h, int M, int K, const void* x, long ldx,
+                     void* q, void* scales, int swizzled, void* stream);
+
+/* out = dequant(A) x dequant(W)^T (`launch_low_latency`: out = a times the
+ * column-major [K, N] weight; bf16 out, float32 accumulation, no scale/bias).
+ *   a        [M, K] E4M3, row stride K, 16-byte aligned.
+ *   a_scales mx_scale_bytes(M, K) bytes, swizzled, 16-byte aligned.
+ *   w        [N, K] E4M3, 16-byte aligned; w_scales swizzled, 32-byte aligned.
+ *   out      [M, N] bf16 row-major, 16-byte aligned; rows >= M untouched.
+ * Constraints: 1 <= M <= 256, N % 128 == 0, K % 128 == 0 (`mxfp8_eligible`:
+ * weight K a multiple of 128), else MX_ERR_UNSUPPORTED / MX_ERR_INVALID_ARG.
+ * flags: MX_FLAG_PDL. */
+int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
+            const void* w, const void* w_scales, void* out, unsigned flags,
+            void* stream);
+
+/* The three projections of a decode step's attention on one stream
+ * (fused_wqa_wkv -> wq_b -> wo_b on the mxfp8 page and in `AttentionStep.run`
+ * of the page "...specialized_decode.attention.step"), every kernel launched
+ * with programmatic dependent launch so its weight read overlaps the previous
+ * kernel (mxfp8 page, module docstring):
+ *   out1 = G1(a1)                         [M, w[0].n]
+ *   a2   = MXFP8(bf16(out1)[:, :g1_cols])  fused into G1's epilogue
+ *   out2 = G2(a2)                         [M, w[1].n], w[1].k == g1_cols
+ *   a3   = MXFP8(bf16(out2))              fused into G2's epilogue, w[2].k == w[1].n
+ *   out  = G3(a3)                         [M, w[2].n] bf16
+ * a2/a2_scales/a3/a3_scales are caller-owned intermediates ([M, K] E4M3 and
+ * mx_scale_bytes(M, K) swizzled bytes each). debug_out1 / debug_out2
+ * (nullable) receive the bf16 out1 / out2. Constraints as mx_gemm, plus
+ * g1_cols % 128 == 0 and g1_cols <= w[0].n. */
+int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales,
+                  const mx_weight w[3], int g1_cols, void* a2, void* a2_scales,
+                  void* a3, void* a3_scales, void* out, void* debug_out1,
+                  void* debug_out2, void* stream);
+
+/* Grouped WO-A with RoPE, writing MXFP8 for wo_b (`dsv41_o_proj` and
+ * `_can_fuse_wo_a` on the page "vllm.models.deepseek_v41.nvidia.ops.o_proj").
+ *   x          [T, >= G*H heads, d_nope + d_rope] bf16; token stride ldx
+ *              elements (ldx >= G*H*(d_nope+d_rope), ldx % 8 == 0), head
+ *              stride d_nope + d_rope; heads gH..gH+H-1 form group g.
+ *   positions  [T] int64 token positions, 0 <= pos < max_pos.
+ *   cos_sin    [max_pos, d_rope] float32: row p = [cos(p f_i) | sin(p f_i)].
+ *   w          [G*R, H*(d_nope+d_rope)] E4M3 (group g = rows gR..gR+R-1),
+ *              w_scales swizzled over those [G*R, H*D/32] scales.
+ *   q, q_scales  out: [T, G*R] E4M3 (row stride G*R) and mx_scale_bytes(T, G*R)
+ *              swizzled bytes: the MXFP8 activation handed to wo_b.
+ *   debug_z    nullable [T, G*R] bf16 z before requantization.
+ *   debug_xq, debug_xs  nullable [T, G*H*D] E4M3 and plain [T, G*H*D/32] scale
+ *              bytes of the RoPE'd, quantized activation the contraction reads.
+ * The rope dims (the last d_rope of each head) are rotated on adjacent pairs
+ * by -pos * f_i in float32 (a' = a c + b s, b' = b c - a s, no fused
+ * multiply-add), quantized per 32 with the nope dims (never rounded to bf16),
+ * contracted per group to R = o_lora_rank with float32 accumulation, rounded
+ * to bf16 and quantized again.
+ * Constraints: d_nope == 448, d_rope == 64, H <= 8, R % 128 == 0,
+ * 1 <= T <= 128; else MX_ERR_UNSUPPORTED (the unfused path's domain).
+ * early_trigger != 0: the dependent kernel (wo_b) may launch right after
+ * this kernel has allocated its tensor memory (`dsv41_o_proj`). */
+int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* positions,
+                 const float* cos_sin, int max_pos, const void* w, const void* w_scales,
+                 int G, int H, int d_nope, int d_rope, int R, void* q, void* q_scales,
+                 void* debug_z, void* debug_xq, void* debug_xs, int early_trigger,
+                 void* stream);
+
+/* Read and clear the device status word: MX_OK, or MX_ERR_TIMEOUT if a kernel
+ * gave up on a bounded wait since the last call. Synchronizes the device. */
+int mx_device_status(mx_handle* h, int* status);
+
+/* Human-readable name of a status code. */
+const char* mx_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MX_H_ */

@@ -1,0 +1,198 @@
+"""Python binding of libmx, the low-batch MXFP8 block-scaled projection library.
+
+Argument marshalling only: every step runs in the CUDA kernels behind the C ABI
+declared in include/mx.h; PyTorch supplies device memory and the current
+stream. There is no fallback: if libmx.so is missing or the device is not a
+compute-capability 10.3 GPU, the calls raise.
+
+Names and argument order follow the C entry points: mx_create, mx_scale_bytes,
+mx_quantize_rows, mx_gemm, mx_gemm_chain, wo_a_grouped, mx_device_status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmx.so")
+
+MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_DEVICE, MX_ERR_CUDA, MX_ERR_TIMEOUT = range(6)
+MX_FLAG_PDL = 1
+
+EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows", "mx_gemm",
+           "mx_gemm_chain", "wo_a_grouped", "mx_device_status", "mx_status_string"]
+
+_vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
+
+
+class MxWeight(ctypes.Structure):
+    _fields_ = [("w", _vp), ("w_scales", _vp), ("n", _i), ("k", _i)]
+
+
+class MxError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmx.so (built by build.build()); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmx.so is not built ({path}); run mxfp8_block_scaled_06_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    lib.mx_create.argtypes = [ctypes.POINTER(_vp), _i]
+    lib.mx_destroy.argtypes = [_vp]
+    lib.mx_scale_bytes.argtypes = [_i, _i]
+    lib.mx_scale_bytes.restype = ctypes.c_size_t
+    lib.mx_quantize_rows.argtypes = [_vp, _i, _i, _vp, _l, _vp, _vp, _i, _vp]
+    lib.mx_gemm.argtypes = [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _u, _vp]
+    lib.mx_gemm_chain.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _vp, _vp]
+    lib.wo_a_grouped.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i,
+                                 _vp, _vp, _vp, _vp, _vp, _i, _vp]
+    lib.mx_device_status.argtypes = [_vp, ctypes.POINTER(_i)]
+    lib.mx_status_string.argtypes = [_i]
+    lib.mx_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().mx_status_string(code).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != MX_OK:
+        raise MxError(rc, what)
+
+
+class Handle:
+    """An mx_handle* bound to one device."""
+
+    def __init__(self, ptr: int, device: int):
+        self.ptr = ptr
+        self.device = device
+
+    def close(self) -> None:
+        if self.ptr:
+            load_library().mx_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def mx_create(device: int = 0) -> Handle:
+    p = _vp()
+    _check(load_library().mx_create(ctypes.byref(p), device), "mx_create")
+    return Handle(p.value, device)
+
+
+def mx_scale_bytes(rows: int, k: int) -> int:
+    return int(load_library().mx_scale_bytes(rows, k))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _empty_u8(shape, device):
+    import torch
+    return torch.empty(shape, dtype=torch.uint8, device=device)
+
+
+def mx_quantize_rows(h: Handle, x, q=None, scales=None, swizzled: bool = True, stream=None):
+    """bf16 [M, K] (row stride x.stride(0)) -> (E4M3 codes uint8 [M, K], scale bytes)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    m, k = x.shape
+    if q is None:
+        q = _empty_u8((m, k), x.device)
+    if scales is None:
+        scales = _empty_u8((mx_scale_bytes(m, k),) if swizzled else (m, k // 32), x.device)
+    _check(load_library().mx_quantize_rows(h.ptr, m, k, _ptr(x), x.stride(0), _ptr(q),
+                                           _ptr(scales), int(swizzled), _stream(stream)),
+           "mx_quantize_rows")
+    return q, scales
+
+
+def mx_gemm(h: Handle, a, a_scales, w, w_scales, out=None, m: int | None = None,
+            pdl: bool = False, stream=None):
+    """out[M, N] bf16 = dequant(a[M, K]) x dequant(w[N, K])^T."""
+    import torch
+    m = a.shape[0] if m is None else m
+    n, k = w.shape
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=w.device)
+    _check(load_library().mx_gemm(h.ptr, m, n, k, _ptr(a), _ptr(a_scales), _ptr(w), _ptr(w_scales),
+                                  _ptr(out), MX_FLAG_PDL if pdl else 0, _stream(stream)), "mx_gemm")
+    return out
+
+
+def mx_gemm_chain(h: Handle, a1, a1_scales, weights, g1_cols: int = 1536, out=None,
+                  a2=None, a2_scales=None, a3=None, a3_scales=None, debug: bool = False,
+                  stream=None) -> dict:
+    """Three projections on one stream with PDL: G1 -> MXFP8 requant of its first
+    g1_cols columns -> G2 -> requant -> G3. weights = [(w, w_scales)] * 3."""
+    import torch
+    m = a1.shape[0]
+    dev = a1.device
+    ws = (MxWeight * 3)(*[MxWeight(_ptr(w), _ptr(s), w.shape[0], w.shape[1]) for w, s in weights])
+    n1, n2, n3 = (w.shape[0] for w, _ in weights)
+    a2 = _empty_u8((m, g1_cols), dev) if a2 is None else a2
+    a2_scales = _empty_u8((mx_scale_bytes(m, g1_cols),), dev) if a2_scales is None else a2_scales
+    a3 = _empty_u8((m, n2), dev) if a3 is None else a3
+    a3_scales = _empty_u8((mx_scale_bytes(m, n2),), dev) if a3_scales is None else a3_scales
+    out = torch.empty((m, n3), dtype=torch.bfloat16, device=dev) if out is None else out
+    d1 = torch.empty((m, n1), dtype=torch.bfloat16, device=dev) if debug else None
+    d2 = torch.empty((m, n2), dtype=torch.bfloat16, device=dev) if debug else None
+    _check(load_library().mx_gemm_chain(h.ptr, m, _ptr(a1), _ptr(a1_scales), ws, g1_cols, _ptr(a2),
+                                        _ptr(a2_scales), _ptr(a3), _ptr(a3_scales), _ptr(out),
+                                        _ptr(d1), _ptr(d2), _stream(stream)), "mx_gemm_chain")
+    return dict(out=out, a2=a2, a2_scales=a2_scales, a3=a3, a3_scales=a3_scales, out1=d1, out2=d2)
+
+
+def wo_a_grouped(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,
+                 heads_per_group: int, o_lora_rank: int, d_nope: int = 448, d_rope: int = 64,
+                 q=None, q_scales=None, debug: bool = False, early_trigger: bool = False,
+                 stream=None) -> dict:
+    """x: bf16 [T, heads, d_nope + d_rope] (token stride x.stride(0)); returns the
+    MXFP8 activation (q, q_scales) for wo_b, plus debug tensors if asked."""
+    import torch
+    t = x.shape[0]
+    dev = x.device
+    cols = n_groups * o_lora_rank
+    kall = n_groups * heads_per_group * (d_nope + d_rope)
+    q = _empty_u8((t, cols), dev) if q is None else q
+    q_scales = _empty_u8((mx_scale_bytes(t, cols),), dev) if q_scales is None else q_scales
+    dz = torch.empty((t, cols), dtype=torch.bfloat16, device=dev) if debug else None
+    dxq = _empty_u8((t, kall), dev) if debug else None
+    dxs = _empty_u8((t, kall // 32), dev) if debug else None
+    _check(load_library().wo_a_grouped(h.ptr, t, _ptr(x), x.stride(0), _ptr(positions),
+                                       _ptr(cos_sin), cos_sin.shape[0], _ptr(w), _ptr(w_scales),
+                                       n_groups, heads_per_group, d_nope, d_rope, o_lora_rank,
+                                       _ptr(q), _ptr(q_scales), _ptr(dz), _ptr(dxq), _ptr(dxs),
+                                       int(early_trigger), _stream(stream)), "wo_a_grouped")
+    return dict(q=q, q_scales=q_scales, z=dz, xq=dxq, xs=dxs)
+
+
+def mx_device_status(h: Handle) -> int:
+    """MX_OK, or the error a kernel recorded since the last call (synchronizes)."""
+    v = _i(0)
+    _check(load_library().mx_device_status(h.ptr, ctypes.byref(v)), "mx_device_status")
+    return v.value

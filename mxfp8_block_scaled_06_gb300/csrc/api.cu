@@ -1,0 +1,279 @@
+// api.cu - the C ABI of libmx (declared in include/mx.h): argument
+// validation (always before any launch), launch plans, TMA tensor maps.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <new>
+
+#include "../../include/mx.h"
+#include "kernels.h"
+
+struct mx_handle {
+  int device;
+  int sm_count;
+  int* d_status;
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+};
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_device(const mx_handle* h) {
+  if (h == nullptr) return MX_ERR_INVALID_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MX_ERR_CUDA;
+  return cur == h->device ? MX_OK : MX_ERR_DEVICE;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+// 2-D uint8 tensor map over a row-major [rows, k] matrix, box {128 bytes, box_rows}
+// with the 128-byte swizzle; out-of-range rows of a box read as zero.
+int make_tmap(const mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, int k,
+              int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = h->encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+int validate_gemm(int M, int N, int K, const void* a, const void* a_scales, const void* w,
+                  const void* w_scales) {
+  if (M < 1 || N < 1 || K < 1) return MX_ERR_INVALID_ARG;
+  if (a == nullptr || a_scales == nullptr || w == nullptr || w_scales == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(a_scales, 16) || !aligned(w, 16) || !aligned(w_scales, 32))
+    return MX_ERR_INVALID_ARG;
+  if (K % 32 != 0) return MX_ERR_INVALID_ARG;
+  if (M > 256 || N % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
+  return MX_OK;
+}
+
+int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
+                const void* w, const void* w_scales, void* out, uint8_t* q, uint8_t* q_scales,
+                int q_cols, bool pdl, cudaStream_t stream) {
+  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count);
+  CUtensorMap tm_w, tm_a;
+  int rc = make_tmap(h, &tm_w, w, N, K, 128);
+  if (rc != MX_OK) return rc;
+  rc = make_tmap(h, &tm_a, a, M, K, plan.mtile);
+  if (rc != MX_OK) return rc;
+  mx::GemmArgs args = {};
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.mtile = plan.mtile;
+  args.stages = plan.stages;
+  args.nchunks = K / 128;
+  args.tmem_cols = plan.tmem_cols;
+  args.a_scales = static_cast<const uint8_t*>(a_scales);
+  args.w_scales = static_cast<const uint8_t*>(w_scales);
+  args.out = out;
+  args.q = q;
+  args.q_scales = q_scales;
+  args.q_cols = q_cols;
+  args.status = h->d_status;
+  return cuda_status(mx::launch_gemm(tm_w, tm_a, args, plan, pdl, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mx_create(mx_handle** out, int device) {
+  if (out == nullptr) return MX_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MX_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return MX_ERR_CUDA;
+  if (major != 10 || minor != 3) return MX_ERR_DEVICE;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return MX_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return MX_ERR_CUDA;
+  mx_handle* h = new (std::nothrow) mx_handle();
+  int rc = MX_OK;
+  if (h == nullptr) {
+    rc = MX_ERR_CUDA;
+  } else {
+    h->device = device;
+    h->sm_count = sms;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      rc = MX_ERR_CUDA;
+    } else {
+      h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      if (mx::set_gemm_attributes() != cudaSuccess || mx::set_wo_a_attributes() != cudaSuccess ||
+          cudaMalloc(&h->d_status, 16) != cudaSuccess ||
+          cudaMemset(h->d_status, 0, 16) != cudaSuccess ||
+          cudaDeviceSynchronize() != cudaSuccess)
+        rc = MX_ERR_CUDA;
+    }
+  }
+  if (rc != MX_OK && h != nullptr) {
+    if (h->d_status) cudaFree(h->d_status);
+    delete h;
+    h = nullptr;
+  }
+  cudaSetDevice(prev);
+  *out = h;
+  return rc;
+}
+
+int mx_destroy(mx_handle* h) {
+  if (h == nullptr) return MX_ERR_INVALID_ARG;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  cudaFree(h->d_status);
+  cudaSetDevice(prev);
+  delete h;
+  return MX_OK;
+}
+
+size_t mx_scale_bytes(int rows, int k) {
+  if (rows < 0 || k < 0 || k % 32 != 0) return 0;
+  const size_t r = (static_cast<size_t>(rows) + 127) / 128 * 128;
+  const size_t c = (static_cast<size_t>(k / 32) + 3) / 4 * 4;
+  return r * c;
+}
+
+int mx_quantize_rows(mx_handle* h, int M, int K, const void* x, long ldx, void* q, void* scales,
+                     int swizzled, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (M < 1 || M > 65536 || K < 32 || K % 32 != 0 || ldx < K || ldx % 8 != 0)
+    return MX_ERR_INVALID_ARG;
+  if (x == nullptr || q == nullptr || scales == nullptr) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q, 16)) return MX_ERR_INVALID_ARG;
+  return cuda_status(mx::launch_quantize_rows(x, ldx, M, K, q, scales, swizzled,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales, const void* w,
+            const void* w_scales, void* out, unsigned flags, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  rc = validate_gemm(M, N, K, a, a_scales, w, w_scales);
+  if (rc != MX_OK) return rc;
+  if (out == nullptr || !aligned(out, 16)) return MX_ERR_INVALID_ARG;
+  if (flags & ~MX_FLAG_PDL) return MX_ERR_INVALID_ARG;
+  return gemm_launch(h, M, N, K, a, a_scales, w, w_scales, out, nullptr, nullptr, 0,
+                     (flags & MX_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream));
+}
+
+int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, const mx_weight w[3],
+                  int g1_cols, void* a2, void* a2_scales, void* a3, void* a3_scales, void* out,
+                  void* debug_out1, void* debug_out2, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (w == nullptr) return MX_ERR_INVALID_ARG;
+  rc = validate_gemm(M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales);
+  if (rc != MX_OK) return rc;
+  rc = validate_gemm(M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales);
+  if (rc != MX_OK) return rc;
+  rc = validate_gemm(M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales);
+  if (rc != MX_OK) return rc;
+  if (g1_cols < 128 || g1_cols % 128 != 0 || g1_cols > w[0].n || w[1].k != g1_cols ||
+      w[2].k != w[1].n)
+    return MX_ERR_INVALID_ARG;
+  if (out == nullptr || !aligned(out, 16)) return MX_ERR_INVALID_ARG;
+  if ((debug_out1 && !aligned(debug_out1, 16)) || (debug_out2 && !aligned(debug_out2, 16)))
+    return MX_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = gemm_launch(h, M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, debug_out1,
+                   static_cast<uint8_t*>(a2), static_cast<uint8_t*>(a2_scales), g1_cols, true, s);
+  if (rc != MX_OK) return rc;
+  rc = gemm_launch(h, M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
+                   static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n, true, s);
+  if (rc != MX_OK) return rc;
+  return gemm_launch(h, M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
+                     nullptr, 0, true, s);
+}
+
+int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* positions,
+                 const float* cos_sin, int max_pos, const void* w, const void* w_scales, int G,
+                 int H, int d_nope, int d_rope, int R, void* q, void* q_scales, void* debug_z,
+                 void* debug_xq, void* debug_xs, int early_trigger, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (x == nullptr || positions == nullptr || cos_sin == nullptr || w == nullptr ||
+      w_scales == nullptr || q == nullptr || q_scales == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (T < 1 || G < 1 || H < 1 || R < 1 || max_pos < 1) return MX_ERR_INVALID_ARG;
+  if (d_nope != 448 || d_rope != 64 || H > 8 || R % 128 != 0 || T > 128) return MX_ERR_UNSUPPORTED;
+  const int D = d_nope + d_rope;
+  if (ldx < static_cast<long>(G) * H * D || ldx % 8 != 0) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(w_scales, 32) || !aligned(q, 16) ||
+      !aligned(q_scales, 16) || !aligned(cos_sin, 16) || !aligned(positions, 8))
+    return MX_ERR_INVALID_ARG;
+  if ((debug_z && !aligned(debug_z, 16)) || (debug_xq && !aligned(debug_xq, 16)))
+    return MX_ERR_INVALID_ARG;
+  const mx::WoaPlan plan = mx::plan_wo_a(T, G, H, R, h->sm_count);
+  CUtensorMap tm_w;
+  rc = make_tmap(h, &tm_w, w, G * R, H * D, 128);
+  if (rc != MX_OK) return rc;
+  mx::WoaArgs args = {};
+  args.T = T;
+  args.G = G;
+  args.H = H;
+  args.R = R;
+  args.D = D;
+  args.mtile = plan.mtile;
+  args.stages = plan.stages;
+  args.tmem_cols = plan.tmem_cols;
+  args.x = static_cast<const uint16_t*>(x);
+  args.ldx = ldx;
+  args.positions = positions;
+  args.cos_sin = cos_sin;
+  args.max_pos = max_pos;
+  args.w_scales = static_cast<const uint8_t*>(w_scales);
+  args.q = static_cast<uint8_t*>(q);
+  args.q_scales = static_cast<uint8_t*>(q_scales);
+  args.debug_z = static_cast<uint16_t*>(debug_z);
+  args.debug_xq = static_cast<uint8_t*>(debug_xq);
+  args.debug_xs = static_cast<uint8_t*>(debug_xs);
+  args.early_trigger = early_trigger;
+  args.status = h->d_status;
+  return cuda_status(mx::launch_wo_a(tm_w, args, plan, static_cast<cudaStream_t>(stream)));
+}
+
+int mx_device_status(mx_handle* h, int* status) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (status == nullptr) return MX_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
+  if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MX_ERR_CUDA;
+  if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return MX_ERR_CUDA;
+  *status = (v & 1) ? MX_ERR_TIMEOUT : (v & 2) ? MX_ERR_INVALID_ARG : MX_OK;
+  return MX_OK;
+}
+
+const char* mx_status_string(int s) {
+  switch (s) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG";
+    case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+    case MX_ERR_DEVICE: return "MX_ERR_DEVICE";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA";
+    case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
+    default: return "MX_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// kernels.h - host-side launchers of the CUDA kernels (internal to libmx).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// ------------------------------------------------------------ quantizer
+cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q, void* scales,
+                                 int swizzled, cudaStream_t stream);
+
+// ------------------------------------------------------------ block-scaled GEMM
+// Plan of one GEMM launch: activation tile (MMA N), K-splits per weight tile
+// (a thread-block cluster along K), pipeline depth, TMEM columns, shared bytes.
+struct GemmPlan {
+  int mtile;
+  int splits;
+  int stages;
+  int tmem_cols;
+  size_t smem;
+};
+
+struct GemmArgs {
+  int M, N, K;
+  int mtile, stages, nchunks, tmem_cols;
+  const uint8_t* a_scales;
+  const uint8_t* w_scales;
+  void* out;          // bf16 [M, N] or null
+  uint8_t* q;         // fused requantization of columns [0, q_cols): E4M3 [M, q_cols]
+  uint8_t* q_scales;  // swizzled scales of q
+  int q_cols;
+  int* status;
+};
+
+GemmPlan plan_gemm(int M, int N, int K, int sm_count);
+cudaError_t set_gemm_attributes();
+cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& args,
+                        const GemmPlan& plan, bool pdl, cudaStream_t stream);
+
+// ------------------------------------------------------------ grouped WO-A
+struct WoaPlan {
+  int mtile;
+  int splits;
+  int stages;
+  int tmem_cols;
+  size_t smem;
+};
+
+struct WoaArgs {
+  int T, G, H, R, D;  // tokens, groups, heads per group, o_lora_rank, head dim (512)
+  int mtile, stages, tmem_cols;
+  const uint16_t* x;  // bf16 bits
+  long ldx;
+  const int64_t* positions;
+  const float* cos_sin;
+  int max_pos;
+  const uint8_t* w_scales;
+  uint8_t* q;
+  uint8_t* q_scales;
+  uint16_t* debug_z;
+  uint8_t* debug_xq;
+  uint8_t* debug_xs;
+  int early_trigger;
+  int* status;
+};
+
+WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count);
+cudaError_t set_wo_a_attributes();
+cudaError_t launch_wo_a(const CUtensorMap& tm_w, const WoaArgs& args, const WoaPlan& plan,
+                        cudaStream_t stream);
+
+}  // namespace mx

@@ -1,0 +1,95 @@
+// quantize.cu - bf16 rows -> MXFP8 (E4M3 + one UE8M0 scale per 32 along K).
+//
+// One warp owns 8 consecutive 32-blocks (256 elements, 512 input bytes) of one
+// row; each lane loads 16 bytes (8 bf16), four lanes form a block and combine
+// their partial amax with two xor-shuffles. Loads are 512-byte coalesced per
+// warp, stores 256 bytes. Padding of the swizzled scale buffer (rows up to a
+// multiple of 128, block columns up to a multiple of 4) is written as zero by
+// the same grid so the whole buffer is defined.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    quantize_rows_kernel(const uint16_t* __restrict__ x, long ldx, int M, int K,
+                         uint8_t* __restrict__ q, uint8_t* __restrict__ scales, int swizzled,
+                         int rows_total, int groups_per_row) {
+  const long gw = static_cast<long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int row = static_cast<int>(gw / groups_per_row);
+  const int grp = static_cast<int>(gw % groups_per_row);
+  if (row >= rows_total) return;  // warp-uniform
+  const int nblk = K >> 5;
+  const int cpad4 = (nblk + 3) & ~3;
+  const int blk = grp * 8 + (lane >> 2);
+  const int sub = lane & 3;
+  const bool valid = row < M && blk < nblk;
+
+  float v[8];
+  float amax = 0.f;
+  uint32_t nonfinite = 0;
+  if (valid) {
+    const uint4 raw =
+        *reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * ldx + blk * 32 + sub * 8);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      nonfinite |= ((w[i] & 0x7F80u) == 0x7F80u) | ((w[i] & 0x7F800000u) == 0x7F800000u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 1);
+  nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 2);
+
+  uint32_t sbyte = 0;
+  if (valid) {
+    uint32_t lo, hi;
+    if (nonfinite) {
+      sbyte = 0xFFu;
+      lo = hi = 0x7F7F7F7Fu;
+    } else {
+      sbyte = mx_scale_byte(amax);
+      const float f = mx_inv_scale(sbyte);
+      lo = cvt_e4m3x2(v[0] * f, v[1] * f) | (cvt_e4m3x2(v[2] * f, v[3] * f) << 16);
+      hi = cvt_e4m3x2(v[4] * f, v[5] * f) | (cvt_e4m3x2(v[6] * f, v[7] * f) << 16);
+    }
+    *reinterpret_cast<uint2*>(q + static_cast<size_t>(row) * K + blk * 32 + sub * 8) =
+        make_uint2(lo, hi);
+  }
+  if (sub == 0) {
+    if (swizzled) {
+      if (blk < cpad4) scales[swz_offset(row, blk, cpad4)] = static_cast<uint8_t>(sbyte);
+    } else if (valid) {
+      scales[static_cast<size_t>(row) * nblk + blk] = static_cast<uint8_t>(sbyte);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q, void* scales,
+                                 int swizzled, cudaStream_t stream) {
+  const int nblk = K / 32;
+  const int cols = swizzled ? ((nblk + 3) & ~3) : nblk;
+  const int groups_per_row = (cols + 7) / 8;
+  const int rows_total = swizzled ? ((M + 127) / 128) * 128 : M;
+  const long warps = static_cast<long>(rows_total) * groups_per_row;
+  const long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  quantize_rows_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
+      static_cast<const uint16_t*>(x), ldx, M, K, static_cast<uint8_t*>(q),
+      static_cast<uint8_t*>(scales), swizzled, rows_total, groups_per_row);
+  return cudaGetLastError();
+}
+
+}  // namespace mx

@@ -1,0 +1,409 @@
+// wo_a.cu - grouped WO-A output projection with inverse RoPE, writing MXFP8.
+//
+// z[t, g R + r] = sum_k dX_g[t, k] dW_g[r, k],  X_g = the H heads of group g,
+// each head = 448 "nope" dims followed by 64 "rope" dims rotated by -pos f_i;
+// q, q_scales = MXFP8(bf16(z)) for the following wo_b GEMM.
+//
+// Grid = (G * R/128 weight tiles) x (K splits); the splits of a tile form a
+// thread-block cluster. Per CTA:
+//  1. weight boxes (TMA, 128 rows x 128 K-bytes, SWIZZLE_128B) and their
+//     scale tiles are issued for the whole ring before the programmatic
+//     grid-dependency wait (with early_trigger, dependents may launch right
+//     after the TMEM allocation, before any load);
+//  2. after the wait, one thread bulk-copies each token's contiguous K-slice
+//     of x (bf16) into shared memory while the others stage the tokens'
+//     cos/sin rows; the 8 warps then rotate the rope pairs in float32 (no
+//     FMA), take each 32-block's amax with two xor-shuffles over the 4 lanes
+//     holding it, and write E4M3 codes straight into the 128-byte-swizzled
+//     K-major operand layout plus 128x4 scale tiles - the activation never
+//     goes to global memory (unless the debug outputs are requested);
+//  3. one thread issues tcgen05.cp + tcgen05.mma.kind::mxf8f6f4.block_scale
+//     per chunk; 4. the cluster reduces the fp32 partials over distributed
+//     shared memory, rounds to bf16 and requantizes each 32-column block.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr uint32_t kWTileBytes = 128 * 128;
+constexpr uint32_t kSfTileBytes = 512;
+constexpr uint32_t kStageBytes = 17408;  // 16 KB weight box + 512 B scales, 1 KB aligned
+constexpr int kTokenBatch = 32;          // tokens whose raw x slices are staged at once
+
+struct WoaLayout {
+  int nmax;                                  // chunks of 128 K per CTA (upper bound)
+  uint32_t ring, act, sfb, xraw, cs, misc, total;
+  __host__ __device__ WoaLayout(int mtile, int stages, int nmax_) : nmax(nmax_) {
+    ring = 0;
+    act = ring + stages * kStageBytes;                         // nmax x [mtile x 128] swizzled
+    sfb = act + static_cast<uint32_t>(nmax) * mtile * 128;     // nmax x 512
+    xraw = sfb + static_cast<uint32_t>(nmax) * kSfTileBytes;   // kTokenBatch x nmax x 256
+    cs = xraw + kTokenBatch * static_cast<uint32_t>(nmax) * 256;  // kTokenBatch x 64 floats
+    misc = cs + kTokenBatch * 64 * 4;
+    total = misc + 8 * (2 * stages + 2) + 16;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    wo_a_kernel(const __grid_constant__ CUtensorMap tm_w, const WoaArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const bp = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_per_group = p.R / 128;
+  const int tile = blockIdx.x;
+  const int g = tile / tiles_per_group;
+  const int rt = tile % tiles_per_group;
+  const int S = gridDim.y;
+  const int split = blockIdx.y;
+  const int kg = p.H * p.D;      // K of one group
+  const int nchunks = kg / 128;
+  const int c_begin = split * nchunks / S;
+  const int n = (split + 1) * nchunks / S - c_begin;
+  const int nmax = (nchunks + S - 1) / S;
+  const int stages = p.stages;
+  const WoaLayout L(p.mtile, stages, nmax);
+
+  const uint32_t bars = base + L.misc;
+  auto wfull = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (stages + s); };
+  const uint32_t accum_bar = bars + 16u * stages;
+  const uint32_t x_bar = accum_bar + 8u;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bp + L.misc + 8 * (2 * stages + 2));
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(wfull(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(accum_bar, 1);
+    mbar_init(x_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sfa_col = (p.mtile + 15) & ~15;
+  const uint32_t sfb_col = sfa_col + 4 * stages;
+  if (p.early_trigger) pdl_launch_dependents();
+
+  auto fail = [&]() {
+    atomicOr(p.status, kStatusTimeout);
+    *abort_flag = 1;
+  };
+
+  const uint64_t pol_w = policy_evict_first();
+  auto issue_w = [&](int i) {
+    const int s = i % stages;
+    const int c = c_begin + i;
+    mbar_expect_tx(wfull(s), kWTileBytes + kSfTileBytes);
+    tma_load_2d(base + L.ring + s * kStageBytes, &tm_w, wfull(s), c * 128, tile * 128, pol_w);
+    bulk_load(base + L.ring + s * kStageBytes + kWTileBytes,
+              p.w_scales + (static_cast<size_t>(tile) * nchunks + c) * kSfTileBytes, kSfTileBytes,
+              wfull(s), pol_w);
+  };
+  const int npre = min(n, stages);
+  int w_issued = 0, x_issued = 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < npre; ++i) issue_w(i);
+    w_issued = npre;
+  }
+  __syncthreads();
+  if (!p.early_trigger) pdl_launch_dependents();
+  pdl_wait();
+
+  // ---------------- prologue: RoPE + MX quantize into the swizzled operand
+  const uint32_t act_tile_bytes = static_cast<uint32_t>(p.mtile) * 128u;
+  {
+    // zero the padding rows [T, mtile) of every chunk tile and all scale tiles
+    const int pad_rows = p.mtile - p.T;
+    for (int idx = threadIdx.x; idx < n * pad_rows * 8; idx += kThreads) {
+      const int i = idx / (pad_rows * 8);
+      const int rem = idx % (pad_rows * 8);
+      const int m = p.T + rem / 8;
+      *reinterpret_cast<uint4*>(bp + L.act + i * act_tile_bytes + m * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    for (int idx = threadIdx.x; idx < n * 32; idx += kThreads)
+      *reinterpret_cast<uint4*>(bp + L.sfb + idx * 16) = make_uint4(0, 0, 0, 0);
+  }
+  const size_t xq_stride = static_cast<size_t>(p.G) * kg;
+  const int units_per_token = n * 16;  // 8-element units in the CTA's K-slice
+  for (int t0 = 0, batch = 0; t0 < p.T; t0 += kTokenBatch, ++batch) {
+    const int tb = min(kTokenBatch, p.T - t0);
+    if (threadIdx.x == 0) {
+      mbar_expect_tx(x_bar, static_cast<uint32_t>(tb) * n * 256u);
+      for (int m = 0; m < tb; ++m) {
+        const uint16_t* src = p.x + static_cast<size_t>(t0 + m) * p.ldx +
+                              static_cast<size_t>(g) * kg + static_cast<size_t>(c_begin) * 128;
+        bulk_load(base + L.xraw + m * nmax * 256, src, n * 256u, x_bar, pol_w);
+      }
+      ++x_issued;
+    }
+    // cos/sin rows of the batch's tokens
+    float* const cs = reinterpret_cast<float*>(bp + L.cs);
+    for (int idx = threadIdx.x; idx < tb * 64; idx += kThreads) {
+      const int m = idx >> 6;
+      long long pos = p.positions[t0 + m];
+      if (pos < 0 || pos >= p.max_pos) {
+        atomicOr(p.status, kStatusBadInput);  // position outside the cache: read row 0
+        pos = 0;
+      }
+      cs[idx] = p.cos_sin[static_cast<size_t>(pos) * 64 + (idx & 63)];
+    }
+    if (!mbar_wait(x_bar, batch & 1)) fail();
+    __syncthreads();
+    const int total = tb * units_per_token;
+    for (int b0 = 0; b0 < total; b0 += kThreads) {
+      const int u = b0 + threadIdx.x;
+      const bool valid = u < total && *abort_flag == 0;
+      const int ml = u / units_per_token;       // token within the batch
+      const int ul = u % units_per_token;       // 8-element unit within the slice
+      const int blk = ul >> 2;                  // 32-block within the slice
+      const int sub = ul & 3;
+      const int kin = c_begin * 128 + ul * 8;   // K index within the group
+      const int d = kin % p.D;
+      float v[8];
+      float amax = 0.f;
+      uint32_t nonfinite = 0;
+      if (valid) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(bp + L.xraw + ml * nmax * 256 + ul * 16);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[2 * i] = __uint_as_float(w4[i] << 16);
+          v[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+        }
+        if (d >= 448) {
+          const float* row = cs + ml * 64;
+          const int p0 = (d - 448) >> 1;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float c = row[p0 + i], s = row[32 + p0 + i];
+            const float a = v[2 * i], b = v[2 * i + 1];
+            v[2 * i] = __fadd_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+            v[2 * i + 1] = __fsub_rn(__fmul_rn(b, c), __fmul_rn(a, s));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          amax = fmaxf(amax, fabsf(v[i]));
+          nonfinite |= !isfinite(v[i]);
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 1);
+      nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 2);
+      if (valid) {
+        uint32_t sbyte, lo, hi;
+        if (nonfinite) {
+          sbyte = 0xFFu;
+          lo = hi = 0x7F7F7F7Fu;
+        } else {
+          sbyte = mx_scale_byte(amax);
+          const float f = mx_inv_scale(sbyte);
+          lo = cvt_e4m3x2(v[0] * f, v[1] * f) | (cvt_e4m3x2(v[2] * f, v[3] * f) << 16);
+          hi = cvt_e4m3x2(v[4] * f, v[5] * f) | (cvt_e4m3x2(v[6] * f, v[7] * f) << 16);
+        }
+        const int m = t0 + ml;
+        const int ci = blk >> 2;                 // chunk within the slice
+        const int kb = (blk & 3) * 32 + sub * 8;  // byte within the 128-byte row
+        const uint32_t off = ci * act_tile_bytes + (m >> 3) * 1024 + (m & 7) * 128 +
+                             (((kb >> 4) ^ (m & 7)) << 4) + (kb & 15);
+        *reinterpret_cast<uint2*>(bp + L.act + off) = make_uint2(lo, hi);
+        if (sub == 0)
+          bp[L.sfb + ci * kSfTileBytes + (m & 31) * 16 + (m >> 5) * 4 + (blk & 3)] =
+              static_cast<uint8_t>(sbyte);
+        if (rt == 0) {
+          const size_t kglob = static_cast<size_t>(g) * kg + kin;
+          if (p.debug_xq)
+            *reinterpret_cast<uint2*>(p.debug_xq + m * xq_stride + kglob) = make_uint2(lo, hi);
+          if (p.debug_xs && sub == 0)
+            p.debug_xs[m * (xq_stride / 32) + kglob / 32] = static_cast<uint8_t>(sbyte);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();  // the next batch reuses the raw slices
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (threadIdx.x == 0) {
+    // ---------------- producer: refill the weight ring
+    for (int i = npre; i < n; ++i) {
+      const int s = i % stages;
+      if (*abort_flag || !mbar_wait(empty(s), ((i / stages) - 1) & 1)) {
+        fail();
+        break;
+      }
+      issue_w(i);
+      ++w_issued;
+    }
+  } else if (threadIdx.x == 32) {
+    // ---------------- MMA issuer
+    for (int i = 0; i < n; ++i) {
+      const int s = i % stages;
+      if (*abort_flag || !mbar_wait(wfull(s), (i / stages) & 1)) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t ta = tmem + sfa_col + 4 * s;
+      const uint32_t tb = tmem + sfb_col + 4 * i;
+      tmem_cp_32x128b_x4(ta, sdesc_sf(base + L.ring + s * kStageBytes + kWTileBytes));
+      tmem_cp_32x128b_x4(tb, sdesc_sf(base + L.sfb + i * kSfTileBytes));
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_mxf8(tmem, sdesc_k_sw128(base + L.ring + s * kStageBytes + 32 * kk),
+                 sdesc_k_sw128(base + L.act + i * act_tile_bytes + 32 * kk),
+                 idesc_mxf8(p.mtile, kk), ta, tb, (i | kk) != 0);
+      tc_commit(empty(s));
+    }
+    tc_commit(accum_bar);
+  }
+
+  // ---------------- epilogue
+  if (!mbar_wait(accum_bar, 0)) fail();
+  tc_fence_after();
+  __syncwarp();
+  float* const red = reinterpret_cast<float*>(bp + L.ring);
+  const bool ok = (*abort_flag == 0);
+  if (ok && warp < 4) {
+    for (int c0 = 0; c0 < p.mtile; c0 += 16) {
+      float v[16];
+      tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + warp * 32 + lane] = v[j];
+    }
+  }
+  tc_fence_before();
+  cluster_sync();
+  if (ok) {
+    const uint32_t red_addr = smem_u32(red);
+    const int qcols = p.G * p.R;
+    const int nwarps = kThreads / 32;
+    for (int item = split + S * warp; item < p.T * 4; item += nwarps * S) {
+      const int m = item >> 2;
+      const int nl = (item & 3) * 32 + lane;
+      const uint32_t off = red_addr + static_cast<uint32_t>(m * 128 + nl) * 4u;
+      float acc = 0.f;
+      for (int r = 0; r < S; ++r) acc += ld_shared_cluster_f32(map_shared_rank(off, r));
+      const __nv_bfloat16 hb = __float2bfloat16_rn(acc);
+      const int col = g * p.R + rt * 128 + nl;
+      if (p.debug_z)
+        p.debug_z[static_cast<size_t>(m) * qcols + col] = __bfloat16_as_ushort(hb);
+      const float v = __bfloat162float(hb);
+      float amax = fabsf(v);
+      uint32_t nonfinite = !isfinite(v);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, o);
+      }
+      uint32_t sbyte, code;
+      if (nonfinite) {
+        sbyte = 0xFFu;
+        code = 0x7Fu;
+      } else {
+        sbyte = mx_scale_byte(amax);
+        code = cvt_e4m3x2(v * mx_inv_scale(sbyte), 0.f) & 0xFFu;
+      }
+      p.q[static_cast<size_t>(m) * qcols + col] = static_cast<uint8_t>(code);
+      if (lane == 0) p.q_scales[swz_offset(m, col >> 5, qcols >> 5)] = static_cast<uint8_t>(sbyte);
+    }
+    if (split == 0) {
+      const int mpad = (p.T + 127) & ~127;
+      for (int idx = threadIdx.x; idx < (mpad - p.T) * 4; idx += kThreads) {
+        const int m = p.T + (idx >> 2);
+        p.q_scales[swz_offset(m, (g * p.R + rt * 128) / 32 + (idx & 3), qcols >> 5)] = 0;
+      }
+    }
+  }
+  cluster_sync();
+
+  if (!ok && threadIdx.x == 0) {
+    for (int i = 0; i < w_issued; ++i) mbar_wait(wfull(i % stages), (i / stages) & 1);
+    for (int b = 0; b < x_issued; ++b) mbar_wait(x_bar, b & 1);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+int pow2_at_least(int v) {
+  int r = 32;
+  while (r < v) r <<= 1;
+  return r;
+}
+
+}  // namespace
+
+WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count) {
+  WoaPlan pl{};
+  pl.mtile = (T + 15) & ~15;
+  const int tiles = G * (R / 128);
+  const int nchunks = H * 512 / 128;
+  int splits = std::max(1, sm_count / std::max(tiles, 1));
+  splits = std::min(splits, std::min(8, nchunks));
+  if (const char* e = getenv("MX_WOA_SPLITS")) {
+    const int v = atoi(e);
+    if (v >= 1 && v <= 8) splits = std::min(v, nchunks);
+  }
+  pl.splits = splits;
+  const int nmax = (nchunks + splits - 1) / splits;
+  int stages = std::min(nmax, 6);
+  // the fp32 partials [mtile][128] are staged in the weight ring
+  while (static_cast<size_t>(stages) * kStageBytes < static_cast<size_t>(pl.mtile) * 512) ++stages;
+  pl.stages = stages;
+  pl.tmem_cols = pow2_at_least(((pl.mtile + 15) & ~15) + 4 * stages + 4 * nmax);
+  const WoaLayout L(pl.mtile, stages, nmax);
+  const int max_res = 512 / pl.tmem_cols;
+  const size_t min_smem = 233472 / static_cast<size_t>(max_res + 1) + 1;
+  pl.smem = std::max(static_cast<size_t>(L.total) + 1024, min_smem);
+  return pl;
+}
+
+cudaError_t set_wo_a_attributes() {
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&wo_a_kernel),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+}
+
+cudaError_t launch_wo_a(const CUtensorMap& tm_w, const WoaArgs& args, const WoaPlan& plan,
+                        cudaStream_t stream) {
+  if (plan.smem > 232448) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(args.G * (args.R / 128), plan.splits, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 1;
+  attrs[0].val.clusterDim.y = plan.splits;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, wo_a_kernel, tm_w, args);
+}
+
+}  // namespace mx

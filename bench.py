@@ -1,0 +1,537 @@
+"""Benchmark of the low-batch MXFP8 decode projections on one GB300 per rank.
+
+Workload (one "step"): the single decode-projection GEMM at M = 1, 2, 4, 8
+activation rows, N = 2048, K = 5120 - each activation arrives as bf16, goes
+through mx_quantize_rows (128x4-swizzled scales) and then mx_gemm (launched
+with programmatic dependent launch). value = algorithmic HBM bytes of the step
+/ step time (GB/s). Weights rotate over enough copies (>= 3x L2) that every
+GEMM streams its weight from HBM. Extras on the same line: per-M GEMM time and
+bandwidth, the three-projection chain (M = 1..64), the grouped WO-A + wo_b
+pair (T = 1, 8, 32), the kernel roofline, an end-to-end number through the
+Python API with host buffers, SM clocks, and the CPU oracle's time on a
+bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --profile gemm|chain|wo_a|sweep   (a few plain launches for ncu)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "small-M MXFP8 GEMM µs & HBM GB/s vs GB300 peak; 3-projection chain µs/step"
+M_LIST = (1, 2, 4, 8)
+N1, K1 = 2048, 5120
+CHAIN_SHAPES = [(2048, 5120), (8192, 1536), (5120, 8192)]
+CHAIN_G1_COLS = 1536
+CHAIN_M = (1, 4, 8, 16, 32, 48, 64)
+WOA = dict(G=4, H=8, R=1024, D=512)
+WOA_T = (1, 8, 32)
+WOB = (5120, 4096)
+SWEEP_M = (64, 96, 128, 192, 256)
+SWEEP_SHAPES = [(8192, 5120), (5120, 8192)]
+
+
+def w_bytes(n, k):
+    return n * k + n * k // 32
+
+
+def gemm_bytes(m, n, k):
+    """Algorithmic bytes of one GEMM: W + W scales + A + A scales + bf16 out."""
+    return w_bytes(n, k) + m * k + m * k // 32 + 2 * m * n
+
+
+def quant_bytes(m, k):
+    return 2 * m * k + m * k + m * k // 32
+
+
+def step_bytes():
+    return sum(gemm_bytes(m, N1, K1) + quant_bytes(m, K1) for m in M_LIST)
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# --------------------------------------------------------------------- device
+class Rig:
+    """Device buffers of the benchmark: rotating weight copies and activations."""
+
+    def __init__(self, torch, mx, h, l2_bytes):
+        self.torch, self.mx, self.h = torch, mx, h
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        self.l2 = l2_bytes
+
+    def copies(self, bytes_per_set):
+        return max(4, -(-3 * self.l2 // bytes_per_set) + 1)
+
+    def weight_set(self, shapes, seed, ncopies):
+        """ncopies independent MXFP8 weight sets (quantized by the library)."""
+        torch, mx = self.torch, self.mx
+        out = []
+        base = []
+        for i, (n, k) in enumerate(shapes):
+            bits = synth.block_scaled_bf16(seed, synth.TAG_W + i, n, k, -6, 6)
+            x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(self.dev)
+            base.append(mx.mx_quantize_rows(self.h, x))
+        for c in range(ncopies):
+            out.append([(q.clone(), s.clone()) for q, s in base])
+        torch.cuda.synchronize()
+        return out
+
+    def activation(self, m, k, seed, umin=-6, umax=6):
+        bits = synth.block_scaled_bf16(seed, synth.TAG_A + m, m, k, umin, umax)
+        return self.torch.from_numpy(bits.view(np.int16)).view(self.torch.bfloat16).to(self.dev)
+
+
+def time_graph(torch, fn, reps, per_graph, stream):
+    """Capture per_graph calls of fn into a CUDA graph, replay it reps times;
+    returns total device milliseconds (CUDA events on the capturing stream)."""
+    with torch.cuda.stream(stream):
+        fn(0)  # make sure everything is initialized outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(per_graph):
+                fn(i)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        g.replay()
+        torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        stop.record(stream)
+    stop.synchronize()
+    return start.elapsed_time(stop), g
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a window."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows if len(r) >= 9 for j in range(4)
+                          if r[5 + j].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sm)}
+
+
+def run_ours(args):
+    import torch
+
+    import mxfp8_block_scaled_06_gb300 as mx
+    from mxfp8_block_scaled_06_gb300 import build as mxbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", init_method="env://")
+    mxbuild.build()
+    torch.cuda.set_device(local)
+    h = mx.mx_create(local)
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    rig = Rig(torch, mx, h, l2)
+    stream = torch.cuda.Stream()
+    pk, pk_kind = peaks()
+    K, W = args.steps, args.warmup
+
+    # ---------------------------------------------------------------- main step
+    nset = rig.copies(w_bytes(N1, K1))
+    wts = rig.weight_set([(N1, K1)], seed=1, ncopies=nset)
+    xs = {m: rig.activation(m, K1, seed=1) for m in M_LIST}
+    qa = {m: (torch.empty((m, K1), dtype=torch.uint8, device=rig.dev),
+              torch.empty(mx.mx_scale_bytes(m, K1), dtype=torch.uint8, device=rig.dev)) for m in M_LIST}
+    outs = {m: torch.empty((m, N1), dtype=torch.bfloat16, device=rig.dev) for m in M_LIST}
+
+    def step(i, quant=True):
+        for j, m in enumerate(M_LIST):
+            wq, ws = wts[(i * len(M_LIST) + j) % nset][0]
+            if quant:
+                mx.mx_quantize_rows(h, xs[m], q=qa[m][0], scales=qa[m][1], stream=stream)
+            mx.mx_gemm(h, qa[m][0], qa[m][1], wq, ws, out=outs[m], pdl=True, stream=stream)
+
+    per_graph = min(K, 100)
+    reps = max(1, K // per_graph)
+    k_eff = reps * per_graph
+    # warm-up: W steps untimed, then a sustained window so the clock sampler sees load
+    for i in range(max(W, 3)):
+        with torch.cuda.stream(stream):
+            step(i)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    t_end = time.time() + 1.0
+    ms_total, g_step = time_graph(torch, step, reps, per_graph, stream)
+    with torch.cuda.stream(stream):
+        while time.time() < t_end:
+            g_step.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    st, sp = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        st.record(stream)
+        for _ in range(reps):
+            g_step.replay()
+        sp.record(stream)
+    sp.synchronize()
+    ms_total = st.elapsed_time(sp)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / k_eff
+    value = world * step_bytes() / (ms_step * 1e-3) / 1e9
+
+    # ------------------------------------------------- per-kernel GEMM timing
+    gemm_us, gemm_gbs = {}, {}
+    for m in M_LIST:
+        def only(i, m=m):
+            wq, ws = wts[i % nset][0]
+            mx.mx_gemm(h, qa[m][0], qa[m][1], wq, ws, out=outs[m], pdl=True, stream=stream)
+        n_launch = 400
+        ms, _ = time_graph(torch, only, 5, n_launch, stream)
+        us = ms * 1e3 / (5 * n_launch)
+        gemm_us[m] = us
+        gemm_gbs[m] = gemm_bytes(m, N1, K1) / (us * 1e-6) / 1e9
+    # dominant kernel: mx_gemm over the step's mix of M
+    ms, _ = time_graph(torch, lambda i: step(i, quant=False), 5, 100, stream)
+    gemm_launch_us = ms * 1e3 / (5 * 100 * len(M_LIST))
+    gemm_mix_bytes = sum(gemm_bytes(m, N1, K1) for m in M_LIST) / len(M_LIST)
+    achieved = gemm_mix_bytes / (gemm_launch_us * 1e-6) / 1e9
+    quant_us = {}
+    for m in (1, 8):
+        ms, _ = time_graph(torch, lambda i, m=m: mx.mx_quantize_rows(
+            h, xs[m], q=qa[m][0], scales=qa[m][1], stream=stream), 5, 200, stream)
+        quant_us[m] = ms * 1e3 / 1000
+
+    # ----------------------------------------------------------------- chain
+    chain = {}
+    if not args.quick:
+        cset = rig.copies(sum(w_bytes(n, k) for n, k in CHAIN_SHAPES))
+        cw = rig.weight_set(CHAIN_SHAPES, seed=2, ncopies=cset)
+        wbytes = sum(w_bytes(n, k) for n, k in CHAIN_SHAPES)
+        for m in CHAIN_M:
+            a1 = rig.activation(m, CHAIN_SHAPES[0][1], seed=2, umin=-4, umax=4)
+            q1 = mx.mx_quantize_rows(h, a1)
+            bufs = dict(out=torch.empty((m, CHAIN_SHAPES[2][0]), dtype=torch.bfloat16, device=rig.dev),
+                        a2=torch.empty((m, CHAIN_G1_COLS), dtype=torch.uint8, device=rig.dev),
+                        a2_scales=torch.empty(mx.mx_scale_bytes(m, CHAIN_G1_COLS), dtype=torch.uint8, device=rig.dev),
+                        a3=torch.empty((m, CHAIN_SHAPES[1][0]), dtype=torch.uint8, device=rig.dev),
+                        a3_scales=torch.empty(mx.mx_scale_bytes(m, CHAIN_SHAPES[1][0]), dtype=torch.uint8, device=rig.dev))
+
+            def run_chain(i, m=m, q1=q1, bufs=bufs):
+                mx.mx_gemm_chain(h, q1[0], q1[1], cw[i % cset], g1_cols=CHAIN_G1_COLS, stream=stream, **bufs)
+            ms, _ = time_graph(torch, run_chain, 5, 60, stream)
+            us = ms * 1e3 / 300
+            chain[m] = {"us": round(us, 3), "weight_gbs": round(wbytes / (us * 1e-6) / 1e9, 1),
+                        "vs_weight_read_at_peak": round(us / (wbytes / (pk["hbm_gbs"] * 1e9) * 1e6), 3)}
+
+    # ------------------------------------------------------- WO-A and wo_b
+    woa = {}
+    if not args.quick:
+        G, H, R, D = WOA["G"], WOA["H"], WOA["R"], WOA["D"]
+        pair = [(G * R, H * D), WOB]
+        wset = rig.copies(sum(w_bytes(n, k) for n, k in pair))
+        ww = rig.weight_set(pair, seed=3, ncopies=wset)
+        cs = torch.from_numpy(synth.rope_cos_sin_cache(65536)).to(rig.dev)
+        for t in WOA_T:
+            xb = synth.normal_bf16(3 + t, synth.TAG_X, (t, G * H, D))
+            x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(rig.dev)
+            pos = torch.from_numpy(synth.positions(3 + t, synth.TAG_POS, t)).to(rig.dev)
+            q = torch.empty((t, G * R), dtype=torch.uint8, device=rig.dev)
+            qs = torch.empty(mx.mx_scale_bytes(t, G * R), dtype=torch.uint8, device=rig.dev)
+            ob = torch.empty((t, WOB[0]), dtype=torch.bfloat16, device=rig.dev)
+
+            def run_woa(i, t=t, x=x, pos=pos, q=q, qs=qs):
+                wq, ws = ww[i % wset][0]
+                mx.wo_a_grouped(h, x, pos, cs, wq, ws, G, H, R, q=q, q_scales=qs, early_trigger=True,
+                                stream=stream)
+
+            def run_pair(i, t=t, x=x, pos=pos, q=q, qs=qs, ob=ob):
+                run_woa(i)
+                wq, ws = ww[i % wset][1]
+                mx.mx_gemm(h, q, qs, wq, ws, out=ob, pdl=True, stream=stream)
+            ms_a, _ = time_graph(torch, run_woa, 5, 60, stream)
+            ms_p, _ = time_graph(torch, run_pair, 5, 60, stream)
+            ua, up = ms_a * 1e3 / 300, ms_p * 1e3 / 300
+            wa = w_bytes(*pair[0])
+            woa[t] = {"wo_a_us": round(ua, 3), "wo_a_weight_gbs": round(wa / (ua * 1e-6) / 1e9, 1),
+                      "wo_a_plus_wo_b_us": round(up, 3),
+                      "pair_weight_gbs": round((wa + w_bytes(*WOB)) / (up * 1e-6) / 1e9, 1)}
+
+    # --------------------------------------------------------------- sweep
+    sweep = {}
+    if args.sweep:
+        for n, k in SWEEP_SHAPES:
+            sset = rig.copies(w_bytes(n, k))
+            sw = rig.weight_set([(n, k)], seed=4, ncopies=sset)
+            for m in SWEEP_M:
+                a = mx.mx_quantize_rows(h, rig.activation(m, k, seed=4))
+                o = torch.empty((m, n), dtype=torch.bfloat16, device=rig.dev)
+                ms, _ = time_graph(torch, lambda i, a=a, o=o: mx.mx_gemm(
+                    h, a[0], a[1], *sw[i % sset][0], out=o, pdl=True, stream=stream), 5, 100, stream)
+                us = ms * 1e3 / 500
+                tf = 2 * m * n * k / (us * 1e-6) / 1e12
+                sweep[f"M{m}_N{n}_K{k}"] = {"us": round(us, 3),
+                                            "gbs": round(gemm_bytes(m, n, k) / (us * 1e-6) / 1e9, 1),
+                                            "tflops": round(tf, 1)}
+
+    # --------------------------------------------------- end to end (host I/O)
+    hx = {m: xs[m].cpu().pin_memory() for m in M_LIST}
+    hout = {m: torch.empty((m, N1), dtype=torch.bfloat16).pin_memory() for m in M_LIST}
+    dx = {m: torch.empty_like(xs[m]) for m in M_LIST}
+    h2d = sum(m * K1 * 2 for m in M_LIST)
+    d2h = sum(m * N1 * 2 for m in M_LIST)
+
+    def e2e_step(i):
+        with torch.cuda.stream(stream):
+            for j, m in enumerate(M_LIST):
+                dx[m].copy_(hx[m], non_blocking=True)
+                q, s = mx.mx_quantize_rows(h, dx[m], q=qa[m][0], scales=qa[m][1], stream=stream)
+                wq, ws = wts[(i * len(M_LIST) + j) % nset][0]
+                mx.mx_gemm(h, q, s, wq, ws, out=outs[m], pdl=True, stream=stream)
+                hout[m].copy_(outs[m], non_blocking=True)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e_steps = min(K, 200)
+    st.record(stream)
+    for i in range(e_steps):
+        e2e_step(i)
+    sp.record(stream)
+    sp.synchronize()
+    e_ms = st.elapsed_time(sp) / e_steps
+    e2e = {"value": round(world * step_bytes() / (e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "path": "Python binding (mx_quantize_rows, mx_gemm) with pinned host input/output copies"}
+
+    status = mx.mx_device_status(h)
+
+    # --------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank != 0:
+        return None
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": args.traffic,
+            "kernel": "gemm_kernel (mx_gemm), mean over M in {1,2,4,8}",
+            "peak_kind": f"{pk_kind} hbm_gbs (burst copy)",
+            "bytes_per_launch": round(gemm_mix_bytes), "launch_us": round(gemm_launch_us, 3)}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": k_eff,
+        "warmup": max(W, 3), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (x e4m3, fp32 accumulate, bf16 out)",
+        "data": "synthetic (SplitMix64/Box-Muller, N(0,1) x 2^U[-6,6] per 32-block)",
+        "config": {"workload": "single decode-projection GEMM: mx_quantize_rows + mx_gemm at M in "
+                               "{1,2,4,8}, N=2048, K=5120 (one step = the four M values)",
+                   "step_bytes": step_bytes(), "pdl": True, "parallelism": f"replicas x{world}",
+                   "l2": f"weights rotate over {nset} copies ({nset * w_bytes(N1, K1) / 1e6:.0f} MB "
+                         f">= 3x L2 {l2 / 1e6:.0f} MB): inputs larger than L2",
+                   "timing": f"CUDA graph of {per_graph} steps replayed {reps}x, CUDA events"},
+        "gemm_us": {str(m): round(v, 3) for m, v in gemm_us.items()},
+        "gemm_gbs": {str(m): round(v, 1) for m, v in gemm_gbs.items()},
+        "gemm_frac_of_peak": {str(m): round(v / pk["hbm_gbs"], 3) for m, v in gemm_gbs.items()},
+        "quantize_us": {str(m): round(v, 3) for m, v in quant_us.items()},
+        "chain_us_per_step": chain, "wo_a": woa, "sweep": sweep,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": k_eff * 2 * len(M_LIST), "clocks": clk, "device_status": status,
+    }
+    return line
+
+
+def cpu_baseline(seconds=15.0):
+    """The oracle as it stands on the host cores: quantize + fp64 dequantized
+    GEMM of the same step, as many whole M values as fit in the time budget."""
+    import oracle
+
+    wbits = synth.block_scaled_bf16(1, synth.TAG_W, N1, K1, -6, 6)
+    wq, ws = oracle.mx_quantize(synth.bf16_bits_to_f64(wbits))  # offline weight quantization
+    done_bytes, t_used, n_gemm = 0, 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        for m in M_LIST:
+            x = synth.bf16_bits_to_f64(synth.block_scaled_bf16(1, synth.TAG_A + m, m, K1, -6, 6))
+            ts = time.perf_counter()
+            aq, as_ = oracle.mx_quantize(x)
+            oracle.round_bf16(oracle.mx_gemm(aq, as_, wq, ws))
+            t_used += time.perf_counter() - ts
+            done_bytes += gemm_bytes(m, N1, K1) + quant_bytes(m, K1)
+            n_gemm += 1
+        if time.perf_counter() - t0 > seconds or n_gemm >= 40:
+            break
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        pass
+    return {"value": round(done_bytes / t_used / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n_gemm} oracle quantize+GEMM calls of the step's M values "
+                      f"({t_used:.1f} s CPU wall); weight quantized once outside the timing",
+            "ms_per_step": round(t_used / (n_gemm / len(M_LIST)) * 1e3, 1)}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on the same workload and metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+
+    wbits = synth.block_scaled_bf16(1, synth.TAG_W, N1, K1, -6, 6)
+    wq, ws = oracle.mx_quantize(synth.bf16_bits_to_f64(wbits))
+    xs = {m: synth.bf16_bits_to_f64(synth.block_scaled_bf16(1, synth.TAG_A + m, m, K1, -6, 6))
+          for m in M_LIST}
+
+    def one_step():
+        for m in M_LIST:
+            aq, as_ = oracle.mx_quantize(xs[m])
+            oracle.round_bf16(oracle.mx_gemm(aq, as_, wq, ws))
+    for _ in range(args.warmup):
+        one_step()
+    steps = max(1, args.steps)
+    t0 = time.perf_counter()
+    budget = 120.0
+    done = 0
+    for _ in range(steps):
+        one_step()
+        done += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    sec = (time.perf_counter() - t0) / done
+    value = step_bytes() / sec / 1e9
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        pass
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": done, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "single decode-projection GEMM: quantize + GEMM at M in "
+                                   "{1,2,4,8}, N=2048, K=5120 (CPU oracle, numpy float64)"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": f"{done} whole steps"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_profile(args):
+    """A few plain (non-graph) launches of one kernel family for ncu."""
+    import torch
+
+    import mxfp8_block_scaled_06_gb300 as mx
+    from mxfp8_block_scaled_06_gb300 import build as mxbuild
+
+    mxbuild.build()
+    torch.cuda.set_device(0)
+    h = mx.mx_create(0)
+    rig = Rig(torch, mx, h, 126 * 2**20)
+    if args.profile == "gemm":
+        w = rig.weight_set([(N1, K1)], 1, 4)
+        for m in (1, 8):
+            q = mx.mx_quantize_rows(h, rig.activation(m, K1, 1))
+            for i in range(3):
+                mx.mx_gemm(h, q[0], q[1], *w[i % 4][0], pdl=True)
+    elif args.profile == "chain":
+        cw = rig.weight_set(CHAIN_SHAPES, 2, 2)
+        for m in (8, 64):
+            q = mx.mx_quantize_rows(h, rig.activation(m, CHAIN_SHAPES[0][1], 2, -4, 4))
+            for i in range(2):
+                mx.mx_gemm_chain(h, q[0], q[1], cw[i % 2], g1_cols=CHAIN_G1_COLS)
+    elif args.profile == "wo_a":
+        G, H, R, D = WOA["G"], WOA["H"], WOA["R"], WOA["D"]
+        ww = rig.weight_set([(G * R, H * D)], 3, 2)
+        cs = torch.from_numpy(synth.rope_cos_sin_cache(65536)).cuda()
+        for t in WOA_T:
+            x = torch.from_numpy(synth.normal_bf16(3, synth.TAG_X, (t, G * H, D)).view(np.int16)).view(torch.bfloat16).cuda()
+            pos = torch.from_numpy(synth.positions(3, synth.TAG_POS, t)).cuda()
+            for i in range(2):
+                mx.wo_a_grouped(h, x, pos, cs, *ww[i % 2][0], G, H, R)
+    elif args.profile == "sweep":
+        for n, k in SWEEP_SHAPES:
+            w = rig.weight_set([(n, k)], 4, 2)
+            for m in (64, 256):
+                q = mx.mx_quantize_rows(h, rig.activation(m, k, 4))
+                for i in range(2):
+                    mx.mx_gemm(h, q[0], q[1], *w[i % 2][0])
+    torch.cuda.synchronize()
+    assert mx.mx_device_status(h) == mx.MX_OK
+    print(json.dumps({"profile": args.profile, "ok": True}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the chain and WO-A extras")
+    ap.add_argument("--sweep", action="store_true", help="also time the M=64..256 row sweep")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per GEMM launch from an ncu capture of the current kernel")
+    ap.add_argument("--profile", default=None, choices=["gemm", "chain", "wo_a", "sweep"])
+    args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

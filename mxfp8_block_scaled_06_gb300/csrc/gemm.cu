@@ -206,8 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = item >> 2;
       const int nl = (item & 3) * 32 + lane;
       const uint32_t off = red_addr + static_cast<uint32_t>(m * 128 + nl) * 4u;
-      float acc = 0.f;
-      for (int r = 0; r < S; ++r) acc += ld_shared_cluster_f32(map_shared_rank(off, r));
+      const float acc = cluster_sum(off, S);
       const __nv_bfloat16 hb = __float2bfloat16_rn(acc);
       const int col = tile * 128 + nl;
       if (out != nullptr) out[static_cast<size_t>(m) * p.N + col] = hb;

@@ -117,10 +117,25 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+// Load from a peer CTA's shared memory. Volatile keeps it after the cluster
+// barrier (volatile asm is never reordered against other volatile asm); no
+// memory clobber, so consecutive loads are issued back to back.
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
+}
+// Sum of the float at shared offset `addr` over cluster ranks 0..S-1 (S <= 8),
+// in rank order; all S loads are issued before the first add.
+__device__ __forceinline__ float cluster_sum(uint32_t addr, int S) {
+  float v[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] = r < S ? ld_shared_cluster_f32(map_shared_rank(addr, r)) : 0.f;
+  float acc = 0.f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    if (r < S) acc += v[r];
+  return acc;
 }
 
 // ------------------------------------------------------------------ tcgen05

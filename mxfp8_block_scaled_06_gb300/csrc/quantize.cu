@@ -20,6 +20,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     quantize_rows_kernel(const uint16_t* __restrict__ x, long ldx, int M, int K,
                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales, int swizzled,
                          int rows_total, int groups_per_row) {
+  // Programmatic dependent launch: let the next kernel (typically a GEMM that
+  // streams its weights first) start now; wait for the previous kernel before
+  // touching memory it may produce or read.
+  pdl_launch_dependents();
+  pdl_wait();
   const long gw = static_cast<long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int row = static_cast<int>(gw / groups_per_row);
@@ -86,10 +91,18 @@ cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q,
   const int rows_total = swizzled ? ((M + 127) / 128) * 128 : M;
   const long warps = static_cast<long>(rows_total) * groups_per_row;
   const long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  quantize_rows_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
-      static_cast<const uint16_t*>(x), ldx, M, K, static_cast<uint8_t*>(q),
-      static_cast<uint8_t*>(scales), swizzled, rows_total, groups_per_row);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kWarpsPerBlock * 32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quantize_rows_kernel, static_cast<const uint16_t*>(x), ldx, M, K,
+                            static_cast<uint8_t*>(q), static_cast<uint8_t*>(scales), swizzled,
+                            rows_total, groups_per_row);
 }
 
 }  // namespace mx

@@ -37,15 +37,15 @@ constexpr uint32_t kStageBytes = 17408;  // 16 KB weight box + 512 B scales, 1 K
 constexpr int kTokenBatch = 32;          // tokens whose raw x slices are staged at once
 
 struct WoaLayout {
-  int nmax;                                  // chunks of 128 K per CTA (upper bound)
   uint32_t ring, act, sfb, xraw, cs, misc, total;
-  __host__ __device__ WoaLayout(int mtile, int stages, int nmax_) : nmax(nmax_) {
+  // tbmax = tokens staged per batch (min(T, kTokenBatch)), nmax = chunks per CTA
+  __host__ __device__ WoaLayout(int mtile, int stages, int nmax, int tbmax) {
     ring = 0;
-    act = ring + stages * kStageBytes;                         // nmax x [mtile x 128] swizzled
-    sfb = act + static_cast<uint32_t>(nmax) * mtile * 128;     // nmax x 512
-    xraw = sfb + static_cast<uint32_t>(nmax) * kSfTileBytes;   // kTokenBatch x nmax x 256
-    cs = xraw + kTokenBatch * static_cast<uint32_t>(nmax) * 256;  // kTokenBatch x 64 floats
-    misc = cs + kTokenBatch * 64 * 4;
+    act = ring + stages * kStageBytes;                              // nmax x [mtile x 128] swizzled
+    sfb = act + static_cast<uint32_t>(nmax) * mtile * 128;          // nmax x 512
+    xraw = sfb + static_cast<uint32_t>(nmax) * kSfTileBytes;        // tbmax x nmax x 256
+    cs = xraw + static_cast<uint32_t>(tbmax) * nmax * 256;          // tbmax x 64 floats
+    misc = cs + static_cast<uint32_t>(tbmax) * 64 * 4;
     total = misc + 8 * (2 * stages + 2) + 16;
   }
 };
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = (split + 1) * nchunks / S - c_begin;
   const int nmax = (nchunks + S - 1) / S;
   const int stages = p.stages;
-  const WoaLayout L(p.mtile, stages, nmax);
+  const WoaLayout L(p.mtile, stages, nmax, min(p.T, kTokenBatch));
 
   const uint32_t bars = base + L.misc;
   auto wfull = [&](int s) { return bars + 8u * s; };
@@ -302,8 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = item >> 2;
       const int nl = (item & 3) * 32 + lane;
       const uint32_t off = red_addr + static_cast<uint32_t>(m * 128 + nl) * 4u;
-      float acc = 0.f;
-      for (int r = 0; r < S; ++r) acc += ld_shared_cluster_f32(map_shared_rank(off, r));
+      const float acc = cluster_sum(off, S);
       const __nv_bfloat16 hb = __float2bfloat16_rn(acc);
       const int col = g * p.R + rt * 128 + nl;
       if (p.debug_z)
@@ -367,17 +366,26 @@ WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count) {
     const int v = atoi(e);
     if (v >= 1 && v <= 8) splits = std::min(v, nchunks);
   }
-  pl.splits = splits;
-  const int nmax = (nchunks + splits - 1) / splits;
-  int stages = std::min(nmax, 6);
-  // the fp32 partials [mtile][128] are staged in the weight ring
-  while (static_cast<size_t>(stages) * kStageBytes < static_cast<size_t>(pl.mtile) * 512) ++stages;
-  pl.stages = stages;
-  pl.tmem_cols = pow2_at_least(((pl.mtile + 15) & ~15) + 4 * stages + 4 * nmax);
-  const WoaLayout L(pl.mtile, stages, nmax);
-  const int max_res = 512 / pl.tmem_cols;
-  const size_t min_smem = 233472 / static_cast<size_t>(max_res + 1) + 1;
-  pl.smem = std::max(static_cast<size_t>(L.total) + 1024, min_smem);
+  const int tbmax = std::min(T, kTokenBatch);
+  // more K-splits (fewer resident activation chunks) and a shallower weight
+  // ring until the CTA fits in shared memory
+  for (; splits <= std::min(8, nchunks); ++splits) {
+    const int nmax = (nchunks + splits - 1) / splits;
+    for (int stages = std::min(nmax, 4); stages >= 1; --stages) {
+      // the fp32 partials [mtile][128] are staged in the weight ring
+      if (static_cast<size_t>(stages) * kStageBytes < static_cast<size_t>(pl.mtile) * 512) break;
+      const WoaLayout L(pl.mtile, stages, nmax, tbmax);
+      if (static_cast<size_t>(L.total) + 1024 > 232448) continue;
+      pl.splits = splits;
+      pl.stages = stages;
+      pl.tmem_cols = pow2_at_least(((pl.mtile + 15) & ~15) + 4 * stages + 4 * nmax);
+      const int max_res = 512 / pl.tmem_cols;
+      const size_t min_smem = 233472 / static_cast<size_t>(max_res + 1) + 1;
+      pl.smem = std::max(static_cast<size_t>(L.total) + 1024, min_smem);
+      return pl;
+    }
+  }
+  pl.smem = 0;  // no plan fits: rejected by launch_wo_a
   return pl;
 }
 
@@ -388,7 +396,7 @@ cudaError_t set_wo_a_attributes() {
 
 cudaError_t launch_wo_a(const CUtensorMap& tm_w, const WoaArgs& args, const WoaPlan& plan,
                         cudaStream_t stream) {
-  if (plan.smem > 232448) return cudaErrorInvalidValue;
+  if (plan.smem == 0 || plan.smem > 232448) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(args.G * (args.R / 128), plan.splits, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -44,8 +44,8 @@ int make_tmap(const mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, in
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-int validate_gemm(int M, int N, int K, const void* a, const void* a_scales, const void* w,
-                  const void* w_scales) {
+int validate_gemm(const mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
+                  const void* w, const void* w_scales) {
   if (M < 1 || N < 1 || K < 1) return MX_ERR_INVALID_ARG;
   if (a == nullptr || a_scales == nullptr || w == nullptr || w_scales == nullptr)
     return MX_ERR_INVALID_ARG;
@@ -53,6 +53,7 @@ int validate_gemm(int M, int N, int K, const void* a, const void* a_scales, cons
     return MX_ERR_INVALID_ARG;
   if (K % 32 != 0) return MX_ERR_INVALID_ARG;
   if (M > 256 || N % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
+  if (mx::plan_gemm(M, N, K, h->sm_count).smem > mx::kMaxDynamicSmem) return MX_ERR_UNSUPPORTED;
   return MX_OK;
 }
 
@@ -167,7 +168,7 @@ int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scal
             const void* w_scales, void* out, unsigned flags, void* stream) {
   int rc = check_device(h);
   if (rc != MX_OK) return rc;
-  rc = validate_gemm(M, N, K, a, a_scales, w, w_scales);
+  rc = validate_gemm(h, M, N, K, a, a_scales, w, w_scales);
   if (rc != MX_OK) return rc;
   if (out == nullptr || !aligned(out, 16)) return MX_ERR_INVALID_ARG;
   if (flags & ~MX_FLAG_PDL) return MX_ERR_INVALID_ARG;
@@ -181,11 +182,11 @@ int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, co
   int rc = check_device(h);
   if (rc != MX_OK) return rc;
   if (w == nullptr) return MX_ERR_INVALID_ARG;
-  rc = validate_gemm(M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales);
+  rc = validate_gemm(h, M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales);
   if (rc != MX_OK) return rc;
-  rc = validate_gemm(M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales);
+  rc = validate_gemm(h, M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales);
   if (rc != MX_OK) return rc;
-  rc = validate_gemm(M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales);
+  rc = validate_gemm(h, M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales);
   if (rc != MX_OK) return rc;
   if (g1_cols < 128 || g1_cols % 128 != 0 || g1_cols > w[0].n || w[1].k != g1_cols ||
       w[2].k != w[1].n)

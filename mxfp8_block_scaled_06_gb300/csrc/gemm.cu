@@ -39,17 +39,32 @@ constexpr int kThreads = 128;
 constexpr uint32_t kWTileBytes = 128 * 128;  // one weight box: 128 rows x 128 K-bytes
 constexpr uint32_t kSfTileBytes = 512;       // one 128x4 scale tile
 
+// Shared-memory carve-up of one CTA: a ring of `stages` (weight box, activation
+// box) pairs, then the weight and activation scale tiles of the CTA's whole
+// K-range (loaded once), then the mbarriers.
 struct Layout {
-  uint32_t a_bytes, sfb_bytes, stage_bytes;
-  __host__ __device__ Layout(int mtile) {
+  uint32_t a_bytes, stage_bytes, ring_bytes, sfa_bytes, sfb_bytes, bars;
+  int stages, nsfb, nmax;
+  __host__ __device__ Layout(int mtile, int stages_, int nmax_) {
+    stages = stages_;
+    nmax = nmax_;
+    nsfb = (mtile + 127) / 128;
     a_bytes = static_cast<uint32_t>(mtile) * 128u;
-    sfb_bytes = kSfTileBytes * static_cast<uint32_t>((mtile + 127) / 128);
-    stage_bytes = (kWTileBytes + a_bytes + kSfTileBytes + sfb_bytes + 1023u) & ~1023u;
+    stage_bytes = (kWTileBytes + a_bytes + 1023u) & ~1023u;
+    ring_bytes = static_cast<uint32_t>(stages) * stage_bytes;
+    sfa_bytes = static_cast<uint32_t>(nmax) * kSfTileBytes;
+    sfb_bytes = static_cast<uint32_t>(nmax * nsfb) * kSfTileBytes;
+    bars = ring_bytes + sfa_bytes + sfb_bytes;
   }
   __host__ __device__ uint32_t w_off(int s) const { return s * stage_bytes; }
   __host__ __device__ uint32_t a_off(int s) const { return s * stage_bytes + kWTileBytes; }
-  __host__ __device__ uint32_t sfa_off(int s) const { return a_off(s) + a_bytes; }
-  __host__ __device__ uint32_t sfb_off(int s) const { return sfa_off(s) + kSfTileBytes; }
+  __host__ __device__ uint32_t sfa_off(int i) const { return ring_bytes + i * kSfTileBytes; }
+  __host__ __device__ uint32_t sfb_off(int rt, int i) const {
+    return ring_bytes + sfa_bytes + (rt * nmax + i) * kSfTileBytes;
+  }
+  // full[stages], empty[stages], sfa, sfb, accum; then TMEM slot and abort flag
+  __host__ __device__ uint32_t bar_bytes() const { return 8u * (2 * stages + 3) + 16u; }
+  __host__ __device__ size_t total() const { return 1024 + bars + bar_bytes(); }
 };
 
 __host__ __device__ inline int tmem_sfa_col(int mtile) { return (mtile + 15) & ~15; }
@@ -71,24 +86,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c_begin = split * p.nchunks / S;
   const int n = (split + 1) * p.nchunks / S - c_begin;
   const int stages = p.stages;
-  const int nsfb = (p.mtile + 127) / 128;
-  const Layout L(p.mtile);
+  const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S);
+  const int nsfb = L.nsfb;
 
-  const uint32_t bars = base + stages * L.stage_bytes;
-  auto wfull = [&](int s) { return bars + 8u * s; };
-  auto afull = [&](int s) { return bars + 8u * (stages + s); };
-  auto empty = [&](int s) { return bars + 8u * (2 * stages + s); };
-  const uint32_t accum_bar = bars + 24u * stages;
-  uint32_t* const tmem_slot =
-      reinterpret_cast<uint32_t*>(base_ptr + stages * L.stage_bytes + 8 * (3 * stages + 1));
+  const uint32_t bars = base + L.bars;
+  // full(s): weight box and activation box of stage s landed (two arrivals);
+  // empty(s): the MMAs reading stage s completed
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (stages + s); };
+  const uint32_t sfa_bar = bars + 16u * stages;
+  const uint32_t sfb_bar = sfa_bar + 8u;
+  const uint32_t accum_bar = sfa_bar + 16u;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L.bars + 8 * (2 * stages + 3));
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(wfull(s), 1);
-      mbar_init(afull(s), 1);
+      mbar_init(full(s), 2);
       mbar_init(empty(s), 1);
     }
+    mbar_init(sfa_bar, 1);
+    mbar_init(sfb_bar, 1);
     mbar_init(accum_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -108,78 +126,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1;
   };
 
-  // ---------------- weights first: they do not depend on the previous kernel
+  // Copies issued by one thread are serviced one after another, so each ring
+  // stage has its own issuing lane: lane s of warp 0 streams the weight boxes of
+  // stage s, lane s of warp 3 the activation boxes, and warp 2 loads the scale
+  // tiles of the whole K-range with one bulk copy per operand.
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_a = policy_evict_last();
-  auto issue_w = [&](int i) {
-    const int s = i % stages;
-    const int c = c_begin + i;
-    mbar_expect_tx(wfull(s), kWTileBytes + kSfTileBytes);
-    tma_load_2d(base + L.w_off(s), &tm_w, wfull(s), c * 128, tile * 128, pol_w);
-    bulk_load(base + L.sfa_off(s),
-              p.w_scales + (static_cast<size_t>(tile) * p.nchunks + c) * kSfTileBytes,
-              kSfTileBytes, wfull(s), pol_w);
+  const bool w_lane = warp == 0 && lane < stages;
+  const bool a_lane = warp == 3 && lane < stages;
+  int last = -1;      // last chunk this lane loaded (weight or activation warps)
+  int issued_n = 0;   // chunks its warp has loaded so far (warp-uniform)
+  auto issue_w = [&](int i, int s) {
+    mbar_expect_tx(full(s), kWTileBytes);
+    tma_load_2d(base + L.w_off(s), &tm_w, full(s), (c_begin + i) * 128, tile * 128, pol_w);
+    last = i;
   };
-  auto issue_a = [&](int i) {
-    const int s = i % stages;
-    const int c = c_begin + i;
-    mbar_expect_tx(afull(s), L.a_bytes + L.sfb_bytes);
-    tma_load_2d(base + L.a_off(s), &tm_a, afull(s), c * 128, 0, pol_a);
-    for (int rt = 0; rt < nsfb; ++rt)
-      bulk_load(base + L.sfb_off(s) + rt * kSfTileBytes,
-                p.a_scales + (static_cast<size_t>(rt) * p.nchunks + c) * kSfTileBytes,
-                kSfTileBytes, afull(s), pol_a);
+  auto issue_a = [&](int i, int s) {
+    mbar_expect_tx(full(s), L.a_bytes);
+    tma_load_2d(base + L.a_off(s), &tm_a, full(s), (c_begin + i) * 128, 0, pol_a);
+    last = i;
   };
-  const int npre = min(n, stages);
-  int w_issued = 0, a_issued = 0;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < npre; ++i) issue_w(i);
-    w_issued = npre;
+
+  // ---------------- before the grid-dependency wait: weights only
+  if (w_lane && lane < n) issue_w(lane, lane);
+  if (warp == 0) issued_n = min(n, stages);
+  if (warp == 2 && lane == 0) {
+    mbar_expect_tx(sfa_bar, static_cast<uint32_t>(n) * kSfTileBytes);
+    bulk_load(base + L.sfa_off(0),
+              p.w_scales + (static_cast<size_t>(tile) * p.nchunks + c_begin) * kSfTileBytes,
+              static_cast<uint32_t>(n) * kSfTileBytes, sfa_bar, pol_w);
   }
-  __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
 
-  if (threadIdx.x == 0) {
-    // ---------------- producer
-    for (int i = 0; i < npre; ++i) issue_a(i);
-    a_issued = npre;
-    for (int i = npre; i < n; ++i) {
-      const int s = i % stages;
-      if (*abort_flag || !mbar_wait(empty(s), ((i / stages) - 1) & 1)) {
-        fail();
-        break;
-      }
-      issue_w(i);
-      ++w_issued;
-      issue_a(i);
-      ++a_issued;
-    }
-  } else if (threadIdx.x == 32) {
-    // ---------------- MMA issuer
-    for (int i = 0; i < n; ++i) {
-      const int s = i % stages;
-      const uint32_t ph = (i / stages) & 1;
-      if (*abort_flag || !mbar_wait(wfull(s), ph) || !mbar_wait(afull(s), ph)) {
-        fail();
-        break;
-      }
-      tc_fence_after();
-      const uint32_t ta = tmem + sfa_col + 4 * s;
-      const uint32_t tb = tmem + sfb_col + 4 * nsfb * s;
-      tmem_cp_32x128b_x4(ta, sdesc_sf(base + L.sfa_off(s)));
-      for (int rt = 0; rt < nsfb; ++rt)
-        tmem_cp_32x128b_x4(tb + 4 * rt, sdesc_sf(base + L.sfb_off(s) + rt * kSfTileBytes));
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_mxf8(tmem, sdesc_k_sw128(base + L.w_off(s) + 32 * kk),
-                 sdesc_k_sw128(base + L.a_off(s) + 32 * kk), idesc_mxf8(p.mtile, kk), ta, tb,
-                 (i | kk) != 0);
-      }
-      tc_commit(empty(s));
-    }
-    tc_commit(accum_bar);
+  // ---------------- activations (written by the previous kernel on the stream)
+  if (a_lane && lane < n) issue_a(lane, lane);
+  if (warp == 3) issued_n = min(n, stages);
+  if (warp == 2 && lane == 1) {
+    mbar_expect_tx(sfb_bar, static_cast<uint32_t>(n * nsfb) * kSfTileBytes);
+    for (int rt = 0; rt < nsfb; ++rt)
+      bulk_load(base + L.sfb_off(rt, 0),
+                p.a_scales + (static_cast<size_t>(rt) * p.nchunks + c_begin) * kSfTileBytes,
+                static_cast<uint32_t>(n) * kSfTileBytes, sfb_bar, pol_a);
   }
+
+  if (warp == 0 || warp == 3) {
+    // ---------------- ring refills (warp-uniform): chunk i re-uses stage
+    // i % stages once the MMAs of chunk i - stages have completed; the issuing
+    // lane rotates, so consecutive copies come from different threads
+    const bool weights = warp == 0;
+    int s = 0, issuer = stages & 31;
+    uint32_t ph = 0, empty_s = empty(0);
+    for (int i = stages; i < n; ++i) {
+      bool freed = mbar_try_wait(empty_s, ph);
+      if (!__all_sync(0xFFFFFFFFu, freed)) freed = *abort_flag == 0 && mbar_wait(empty_s, ph);
+      if (!__all_sync(0xFFFFFFFFu, freed)) {
+        if (lane == 0) fail();
+        break;
+      }
+      if (lane == issuer) {
+        if (weights) issue_w(i, s);
+        else issue_a(i, s);
+      }
+      issued_n = i + 1;
+      __syncwarp();
+      if (++issuer == 32) issuer = 0;
+      if (++s == stages) {
+        s = 0;
+        ph ^= 1u;
+        empty_s = empty(0);
+      } else {
+        empty_s += 8;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA warp. The whole warp walks the ring (waits, counters,
+    // descriptors: warp-uniform values) and one elected lane issues the tcgen05
+    // ops. The issue latency of that one instruction stream bounds the loop, so
+    // the smem descriptors advance by 32-bit adds on their low halves (address
+    // field in 16-byte units) and stage, phase, barrier and TMEM addresses are
+    // running values rather than divisions and products.
+    const uint64_t wd = sdesc_k_sw128(base + L.w_off(0));
+    const uint64_t ad = sdesc_k_sw128(base + L.a_off(0));
+    const uint64_t fd = sdesc_sf(base + L.sfa_off(0));
+    const uint64_t gd = sdesc_sf(base + L.sfb_off(0, 0));
+    const uint32_t op_hi = static_cast<uint32_t>(wd >> 32), sf_hi = static_cast<uint32_t>(fd >> 32);
+    const uint32_t stage_units = L.stage_bytes >> 4;
+    const uint32_t rt_units = (static_cast<uint32_t>(L.nmax) * kSfTileBytes) >> 4;
+    const uint32_t id0 = idesc_mxf8(p.mtile, 0), id1 = idesc_mxf8(p.mtile, 1);
+    const uint32_t id2 = idesc_mxf8(p.mtile, 2), id3 = idesc_mxf8(p.mtile, 3);
+    // every wait below is taken by all lanes and decided by a warp vote, so the
+    // warp stays converged for elect.sync and leaves the loop together
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfa_bar, 0) && mbar_wait(sfb_bar, 0))) {
+      if (lane == 0) fail();
+    } else {
+      uint32_t w_lo = static_cast<uint32_t>(wd), a_lo = static_cast<uint32_t>(ad);
+      uint32_t f_lo = static_cast<uint32_t>(fd), g_lo = static_cast<uint32_t>(gd);
+      uint32_t ta = tmem + sfa_col, tb = tmem + sfb_col;
+      uint32_t full_s = full(0), empty_s = empty(0);
+      uint32_t ph = 0;
+      int s = 0;
+      for (int i = 0; i < n; ++i) {
+        bool landed = mbar_try_wait(full_s, ph);
+        if (!__all_sync(0xFFFFFFFFu, landed)) landed = *abort_flag == 0 && mbar_wait(full_s, ph);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+          if (lane == 0) fail();
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          tmem_cp_32x128b_x4_lh(ta, f_lo, sf_hi);
+          tmem_cp_32x128b_x4_lh(tb, g_lo, sf_hi);
+          if (nsfb > 1) tmem_cp_32x128b_x4_lh(tb + 4, g_lo + rt_units, sf_hi);
+          mma_mxf8_lh(tmem, w_lo, op_hi, a_lo, op_hi, id0, ta, tb, i != 0);
+          mma_mxf8_lh(tmem, w_lo + 2, op_hi, a_lo + 2, op_hi, id1, ta, tb, 1);
+          mma_mxf8_lh(tmem, w_lo + 4, op_hi, a_lo + 4, op_hi, id2, ta, tb, 1);
+          mma_mxf8_lh(tmem, w_lo + 6, op_hi, a_lo + 6, op_hi, id3, ta, tb, 1);
+          if (i + stages < n) tc_commit(empty_s);  // only stages that will be refilled
+        }
+        __syncwarp();
+        f_lo += kSfTileBytes >> 4;
+        g_lo += kSfTileBytes >> 4;
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+          w_lo = static_cast<uint32_t>(wd);
+          a_lo = static_cast<uint32_t>(ad);
+          ta = tmem + sfa_col;
+          tb = tmem + sfb_col;
+          full_s = full(0);
+          empty_s = empty(0);
+        } else {
+          w_lo += stage_units;
+          a_lo += stage_units;
+          ta += 4;
+          tb += 4 * nsfb;
+          full_s += 8;
+          empty_s += 8;
+        }
+      }
+    }
+    if (elect_one()) tc_commit(accum_bar);
+    __syncwarp();
+  }
+  __syncwarp();
 
   // ---------------- epilogue: TMEM -> shared partials
   if (!mbar_wait(accum_bar, 0)) fail();
@@ -243,10 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
 
   // ---------------- teardown
-  if (!ok && threadIdx.x == 0) {
-    // wait (bounded) for every copy this CTA issued, so none lands after exit
-    for (int i = 0; i < w_issued; ++i) mbar_wait(wfull(i % stages), (i / stages) & 1);
-    for (int i = 0; i < a_issued; ++i) mbar_wait(afull(i % stages), (i / stages) & 1);
+  if (*abort_flag != 0) {
+    // wait (bounded) for the copies still in flight, so none lands after exit:
+    // per stage, the last chunk loaded into it (an earlier one in the same stage
+    // had landed before the stage was refilled)
+    if (last >= 0 && last + stages >= issued_n) mbar_wait(full(last % stages), (last / stages) & 1);
+    if (warp == 2 && lane == 0) mbar_wait(sfa_bar, 0);
+    if (warp == 2 && lane == 1) mbar_wait(sfb_bar, 0);
   }
   __syncthreads();
   if (warp == 0) {
@@ -268,34 +361,44 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count) {
   pl.mtile = (M + 15) & ~15;
   const int tiles = N / 128;
   const int nchunks = K / 128;
+  const int nsfb = (pl.mtile + 127) / 128;
   int splits = std::max(1, sm_count / std::max(tiles, 1));
   splits = std::min(splits, std::min(8, nchunks));
   if (const char* e = getenv("MX_SPLITS")) {
     const int v = atoi(e);
     if (v >= 1 && v <= 8) splits = std::min(v, nchunks);
   }
+  // the scale tiles of a CTA's K-range stay resident: at most 48 KB of them
+  auto scale_bytes = [&](int sp) {
+    return static_cast<size_t>((nchunks + sp - 1) / sp) * kSfTileBytes * (1 + nsfb);
+  };
+  while (splits < std::min(8, nchunks) && scale_bytes(splits) > 48 * 1024) ++splits;
   pl.splits = splits;
   const int per_cta = (nchunks + splits - 1) / splits;
-  const Layout L(pl.mtile);
-  const size_t budget = 96 * 1024;
-  int stages = static_cast<int>(budget / L.stage_bytes);
-  stages = std::max(2, std::min(stages, 8));
+  const Layout L1(pl.mtile, 1, per_cta);
+  const size_t scales = L1.sfa_bytes + L1.sfb_bytes;
+  // Short K-ranges (all chunks in flight at once): about 100 KB per CTA, so the
+  // next kernel's CTAs fit beside this one. Long ones: a deep ring (more bytes
+  // in flight per SM) matters more than that overlap.
+  const size_t budget = per_cta <= 8 ? 100 * 1024 : 180 * 1024;
+  int stages = budget > scales ? static_cast<int>((budget - scales) / L1.stage_bytes) : 0;
+  stages = std::max(2, std::min(stages, 10));
   if (const char* e = getenv("MX_STAGES")) {
     const int v = atoi(e);
     if (v >= 1 && v <= 12) stages = v;
   }
   stages = std::min(stages, per_cta);
-  // the epilogue stages the fp32 partials [mtile][128] in the pipeline buffers
-  while (static_cast<size_t>(stages) * L.stage_bytes < static_cast<size_t>(pl.mtile) * 512) ++stages;
+  // the epilogue stages the fp32 partials [mtile][128] over the ring and scale tiles
+  while (static_cast<size_t>(stages) * L1.stage_bytes + scales < static_cast<size_t>(pl.mtile) * 512)
+    ++stages;
   pl.stages = stages;
-  const int nsfb = (pl.mtile + 127) / 128;
-  pl.tmem_cols = pow2_at_least(tmem_sfa_col(pl.mtile) + 4 * stages + 4 * nsfb * stages);
-  size_t smem = 1024 + static_cast<size_t>(stages) * L.stage_bytes + 8 * (3 * stages + 1) + 16;
+  pl.tmem_cols = pow2_at_least(tmem_sfa_col(pl.mtile) + 4 * stages * (1 + nsfb));
+  const Layout L(pl.mtile, stages, per_cta);
   // CTAs that can share an SM must fit their TMEM together: ask for enough
   // shared memory that at most 512 / tmem_cols of them are resident.
   const int max_res = 512 / pl.tmem_cols;
   const size_t min_smem = 233472 / static_cast<size_t>(max_res + 1) + 1;
-  pl.smem = std::max(smem, min_smem);
+  pl.smem = std::max(L.total(), min_smem);
   return pl;
 }
 
@@ -303,7 +406,8 @@ cudaError_t set_gemm_attributes() {
   const void* ks[2] = {reinterpret_cast<const void*>(&gemm_kernel<false>),
                        reinterpret_cast<const void*>(&gemm_kernel<true>)};
   for (const void* k : ks) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMaxDynamicSmem));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -311,6 +415,7 @@ cudaError_t set_gemm_attributes() {
 
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& args,
                         const GemmPlan& plan, bool pdl, cudaStream_t stream) {
+  if (plan.smem > kMaxDynamicSmem) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(args.N / 128, plan.splits, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -7,6 +7,9 @@
 
 namespace mx {
 
+// Largest dynamic shared memory one CTA may ask for on sm_103a.
+constexpr size_t kMaxDynamicSmem = 232448;
+
 // ------------------------------------------------------------ quantizer
 cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q, void* scales,
                                  int swizzled, cudaStream_t stream);

@@ -138,6 +138,19 @@ __device__ __forceinline__ float cluster_sum(uint32_t addr, int S) {
   return acc;
 }
 
+// ------------------------------------------------------------------ warp
+// True in exactly one active lane of a converged warp (elect.sync); code around
+// it stays warp-uniform, so its values can live in uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------ tcgen05
 // Warp-wide: allocate ncols (power of two >= 32) TMEM columns, address -> smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -202,6 +215,29 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
       "[%6], p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
+}
+// The same MMA with each smem descriptor passed as its two 32-bit halves: a
+// loop that walks a ring only changes the low half (the address field), so it
+// advances descriptors with 32-bit adds and keeps the high halves in registers.
+__device__ __forceinline__ void mma_mxf8_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                            uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], da, db, %6, [%7], "
+      "[%8], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(accumulate), "r"(idesc), "r"(sfa_tmem),
+      "r"(sfb_tmem)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4_lh(uint32_t taddr, uint32_t lo, uint32_t hi) {
+  asm volatile("{\n\t.reg .b64 d;\n\tmov.b64 d, {%1, %2};\n\t"
+               "tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], d;\n\t}" ::"r"(taddr),
+               "r"(lo), "r"(hi)
+               : "memory");
 }
 // Copy a 32x128-bit smem tile into TMEM lanes 0-31, replicated into all four
 // 32-lane quarters (4 columns).

@@ -6,20 +6,23 @@
 //
 // Grid = (G * R/128 weight tiles) x (K splits); the splits of a tile form a
 // thread-block cluster. Per CTA:
-//  1. weight boxes (TMA, 128 rows x 128 K-bytes, SWIZZLE_128B) and their
-//     scale tiles are issued for the whole ring before the programmatic
-//     grid-dependency wait (with early_trigger, dependents may launch right
-//     after the TMEM allocation, before any load);
-//  2. after the wait, one thread bulk-copies each token's contiguous K-slice
-//     of x (bf16) into shared memory while the others stage the tokens'
+//  1. weight boxes (TMA, 128 rows x 128 K-bytes, SWIZZLE_128B) are issued for
+//     the whole ring, one lane per box, and the scale tiles of the CTA's K-range
+//     with one bulk copy, before the programmatic grid-dependency wait (with
+//     early_trigger, dependents may launch right after the TMEM allocation);
+//  2. after the wait, one lane per token bulk-copies the token's contiguous
+//     K-slice of x (bf16) into shared memory while the others stage the tokens'
 //     cos/sin rows; the 8 warps then rotate the rope pairs in float32 (no
 //     FMA), take each 32-block's amax with two xor-shuffles over the 4 lanes
 //     holding it, and write E4M3 codes straight into the 128-byte-swizzled
 //     K-major operand layout plus 128x4 scale tiles - the activation never
 //     goes to global memory (unless the debug outputs are requested);
-//  3. one thread issues tcgen05.cp + tcgen05.mma.kind::mxf8f6f4.block_scale
-//     per chunk; 4. the cluster reduces the fp32 partials over distributed
-//     shared memory, rounds to bf16 and requantizes each 32-column block.
+//  3. the MMA warp walks the chunks warp-uniformly and an elected lane issues
+//     tcgen05.cp + tcgen05.mma.kind::mxf8f6f4.block_scale; weight refills come
+//     from a warp-uniform loop whose issuing lane rotates (copies issued by one
+//     thread are serviced one after another); 4. the cluster reduces the fp32
+//     partials over distributed shared memory, rounds to bf16 and requantizes
+//     each 32-column block.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -33,20 +36,21 @@ namespace {
 constexpr int kThreads = 256;
 constexpr uint32_t kWTileBytes = 128 * 128;
 constexpr uint32_t kSfTileBytes = 512;
-constexpr uint32_t kStageBytes = 17408;  // 16 KB weight box + 512 B scales, 1 KB aligned
+constexpr uint32_t kStageBytes = 16384;  // one weight box
 constexpr int kTokenBatch = 32;          // tokens whose raw x slices are staged at once
 
 struct WoaLayout {
-  uint32_t ring, act, sfb, xraw, cs, misc, total;
+  uint32_t ring, act, sfb, sfa, xraw, cs, misc, total;
   // tbmax = tokens staged per batch (min(T, kTokenBatch)), nmax = chunks per CTA
   __host__ __device__ WoaLayout(int mtile, int stages, int nmax, int tbmax) {
     ring = 0;
     act = ring + stages * kStageBytes;                              // nmax x [mtile x 128] swizzled
     sfb = act + static_cast<uint32_t>(nmax) * mtile * 128;          // nmax x 512
-    xraw = sfb + static_cast<uint32_t>(nmax) * kSfTileBytes;        // tbmax x nmax x 256
+    sfa = sfb + static_cast<uint32_t>(nmax) * kSfTileBytes;         // nmax x 512 (weight scales)
+    xraw = sfa + static_cast<uint32_t>(nmax) * kSfTileBytes;        // tbmax x nmax x 256
     cs = xraw + static_cast<uint32_t>(tbmax) * nmax * 256;          // tbmax x 64 floats
     misc = cs + static_cast<uint32_t>(tbmax) * 64 * 4;
-    total = misc + 8 * (2 * stages + 2) + 16;
+    total = misc + 8 * (2 * stages + 3) + 16;
   }
 };
 
@@ -78,7 +82,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty = [&](int s) { return bars + 8u * (stages + s); };
   const uint32_t accum_bar = bars + 16u * stages;
   const uint32_t x_bar = accum_bar + 8u;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bp + L.misc + 8 * (2 * stages + 2));
+  const uint32_t sfa_bar = accum_bar + 16u;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bp + L.misc + 8 * (2 * stages + 3));
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
@@ -88,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(accum_bar, 1);
     mbar_init(x_bar, 1);
+    mbar_init(sfa_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w);
@@ -107,22 +113,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   const uint64_t pol_w = policy_evict_first();
-  auto issue_w = [&](int i) {
-    const int s = i % stages;
-    const int c = c_begin + i;
-    mbar_expect_tx(wfull(s), kWTileBytes + kSfTileBytes);
-    tma_load_2d(base + L.ring + s * kStageBytes, &tm_w, wfull(s), c * 128, tile * 128, pol_w);
-    bulk_load(base + L.ring + s * kStageBytes + kWTileBytes,
-              p.w_scales + (static_cast<size_t>(tile) * nchunks + c) * kSfTileBytes, kSfTileBytes,
-              wfull(s), pol_w);
+  int last = -1;      // last chunk whose weight box this lane loaded (warp 0)
+  int issued_n = 0;   // weight boxes warp 0 has loaded so far (warp-uniform)
+  auto issue_w = [&](int i, int s) {
+    mbar_expect_tx(wfull(s), kWTileBytes);
+    tma_load_2d(base + L.ring + s * kStageBytes, &tm_w, wfull(s), (c_begin + i) * 128, tile * 128,
+                pol_w);
+    last = i;
   };
-  const int npre = min(n, stages);
-  int w_issued = 0, x_issued = 0;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < npre; ++i) issue_w(i);
-    w_issued = npre;
+  if (warp == 0) {
+    if (lane < min(n, stages)) issue_w(lane, lane);
+    issued_n = min(n, stages);
   }
-  __syncthreads();
+  if (warp == 2 && lane == 0) {
+    mbar_expect_tx(sfa_bar, static_cast<uint32_t>(n) * kSfTileBytes);
+    bulk_load(base + L.sfa, p.w_scales + (static_cast<size_t>(tile) * nchunks + c_begin) * kSfTileBytes,
+              static_cast<uint32_t>(n) * kSfTileBytes, sfa_bar, pol_w);
+  }
+  int x_batches = 0;
   if (!p.early_trigger) pdl_launch_dependents();
   pdl_wait();
 
@@ -145,14 +153,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int units_per_token = n * 16;  // 8-element units in the CTA's K-slice
   for (int t0 = 0, batch = 0; t0 < p.T; t0 += kTokenBatch, ++batch) {
     const int tb = min(kTokenBatch, p.T - t0);
-    if (threadIdx.x == 0) {
-      mbar_expect_tx(x_bar, static_cast<uint32_t>(tb) * n * 256u);
-      for (int m = 0; m < tb; ++m) {
-        const uint16_t* src = p.x + static_cast<size_t>(t0 + m) * p.ldx +
+    if (warp == 0) {
+      // one lane per token (tb <= 32)
+      if (lane == 0) mbar_expect_tx(x_bar, static_cast<uint32_t>(tb) * n * 256u);
+      __syncwarp();
+      if (lane < tb) {
+        const uint16_t* src = p.x + static_cast<size_t>(t0 + lane) * p.ldx +
                               static_cast<size_t>(g) * kg + static_cast<size_t>(c_begin) * 128;
-        bulk_load(base + L.xraw + m * nmax * 256, src, n * 256u, x_bar, pol_w);
+        bulk_load(base + L.xraw + lane * nmax * 256, src, n * 256u, x_bar, pol_w);
       }
-      ++x_issued;
+      x_batches = batch + 1;
     }
     // cos/sin rows of the batch's tokens
     float* const cs = reinterpret_cast<float*>(bp + L.cs);
@@ -244,39 +254,91 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_proxy_async_smem();
   __syncthreads();
 
-  if (threadIdx.x == 0) {
-    // ---------------- producer: refill the weight ring
-    for (int i = npre; i < n; ++i) {
-      const int s = i % stages;
-      if (*abort_flag || !mbar_wait(empty(s), ((i / stages) - 1) & 1)) {
-        fail();
+  if (warp == 0) {
+    // ---------------- weight ring refills (warp-uniform, rotating issuing lane):
+    // chunk i re-uses stage i % stages once the MMAs of chunk i - stages completed
+    int s = 0, issuer = stages & 31;
+    uint32_t ph = 0, empty_s = empty(0);
+    for (int i = stages; i < n; ++i) {
+      bool freed = mbar_try_wait(empty_s, ph);
+      if (!__all_sync(0xFFFFFFFFu, freed)) freed = *abort_flag == 0 && mbar_wait(empty_s, ph);
+      if (!__all_sync(0xFFFFFFFFu, freed)) {
+        if (lane == 0) fail();
         break;
       }
-      issue_w(i);
-      ++w_issued;
-    }
-  } else if (threadIdx.x == 32) {
-    // ---------------- MMA issuer
-    for (int i = 0; i < n; ++i) {
-      const int s = i % stages;
-      if (*abort_flag || !mbar_wait(wfull(s), (i / stages) & 1)) {
-        fail();
-        break;
+      if (lane == issuer) issue_w(i, s);
+      issued_n = i + 1;
+      __syncwarp();
+      if (++issuer == 32) issuer = 0;
+      if (++s == stages) {
+        s = 0;
+        ph ^= 1u;
+        empty_s = empty(0);
+      } else {
+        empty_s += 8;
       }
-      tc_fence_after();
-      const uint32_t ta = tmem + sfa_col + 4 * s;
-      const uint32_t tb = tmem + sfb_col + 4 * i;
-      tmem_cp_32x128b_x4(ta, sdesc_sf(base + L.ring + s * kStageBytes + kWTileBytes));
-      tmem_cp_32x128b_x4(tb, sdesc_sf(base + L.sfb + i * kSfTileBytes));
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_mxf8(tmem, sdesc_k_sw128(base + L.ring + s * kStageBytes + 32 * kk),
-                 sdesc_k_sw128(base + L.act + i * act_tile_bytes + 32 * kk),
-                 idesc_mxf8(p.mtile, kk), ta, tb, (i | kk) != 0);
-      tc_commit(empty(s));
     }
-    tc_commit(accum_bar);
+  } else if (warp == 1) {
+    // ---------------- MMA warp: warp-uniform walk, one elected lane issues; the
+    // smem descriptors advance by 32-bit adds on their low halves
+    const uint64_t wd = sdesc_k_sw128(base + L.ring);
+    const uint64_t ad = sdesc_k_sw128(base + L.act);
+    const uint64_t fd = sdesc_sf(base + L.sfa);
+    const uint64_t gd = sdesc_sf(base + L.sfb);
+    const uint32_t op_hi = static_cast<uint32_t>(wd >> 32), sf_hi = static_cast<uint32_t>(fd >> 32);
+    const uint32_t id0 = idesc_mxf8(p.mtile, 0), id1 = idesc_mxf8(p.mtile, 1);
+    const uint32_t id2 = idesc_mxf8(p.mtile, 2), id3 = idesc_mxf8(p.mtile, 3);
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfa_bar, 0))) {
+      if (lane == 0) fail();
+    } else {
+      uint32_t w_lo = static_cast<uint32_t>(wd), a_lo = static_cast<uint32_t>(ad);
+      uint32_t f_lo = static_cast<uint32_t>(fd), g_lo = static_cast<uint32_t>(gd);
+      uint32_t ta = tmem + sfa_col, tb = tmem + sfb_col;
+      uint32_t full_s = wfull(0), empty_s = empty(0);
+      uint32_t ph = 0;
+      int s = 0;
+      for (int i = 0; i < n; ++i) {
+        bool landed = mbar_try_wait(full_s, ph);
+        if (!__all_sync(0xFFFFFFFFu, landed)) landed = *abort_flag == 0 && mbar_wait(full_s, ph);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+          if (lane == 0) fail();
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          tmem_cp_32x128b_x4_lh(ta, f_lo, sf_hi);
+          tmem_cp_32x128b_x4_lh(tb, g_lo, sf_hi);
+          mma_mxf8_lh(tmem, w_lo, op_hi, a_lo, op_hi, id0, ta, tb, i != 0);
+          mma_mxf8_lh(tmem, w_lo + 2, op_hi, a_lo + 2, op_hi, id1, ta, tb, 1);
+          mma_mxf8_lh(tmem, w_lo + 4, op_hi, a_lo + 4, op_hi, id2, ta, tb, 1);
+          mma_mxf8_lh(tmem, w_lo + 6, op_hi, a_lo + 6, op_hi, id3, ta, tb, 1);
+          if (i + stages < n) tc_commit(empty_s);  // only stages that will be refilled
+        }
+        __syncwarp();
+        f_lo += kSfTileBytes >> 4;
+        g_lo += kSfTileBytes >> 4;
+        a_lo += act_tile_bytes >> 4;
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+          w_lo = static_cast<uint32_t>(wd);
+          ta = tmem + sfa_col;
+          tb = tmem + sfb_col;
+          full_s = wfull(0);
+          empty_s = empty(0);
+        } else {
+          w_lo += kStageBytes >> 4;
+          ta += 4;
+          tb += 4;
+          full_s += 8;
+          empty_s += 8;
+        }
+      }
+    }
+    if (elect_one()) tc_commit(accum_bar);
+    __syncwarp();
   }
+  __syncwarp();
 
   // ---------------- epilogue
   if (!mbar_wait(accum_bar, 0)) fail();
@@ -336,9 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cluster_sync();
 
-  if (!ok && threadIdx.x == 0) {
-    for (int i = 0; i < w_issued; ++i) mbar_wait(wfull(i % stages), (i / stages) & 1);
-    for (int b = 0; b < x_issued; ++b) mbar_wait(x_bar, b & 1);
+  if (*abort_flag != 0) {
+    // wait (bounded) for the copies still in flight, so none lands after exit
+    if (last >= 0 && last + stages >= issued_n) mbar_wait(wfull(last % stages), (last / stages) & 1);
+    if (warp == 0 && lane == 0 && x_batches > 0) mbar_wait(x_bar, (x_batches - 1) & 1);
+    if (warp == 2 && lane == 0) mbar_wait(sfa_bar, 0);
   }
   __syncthreads();
   if (warp == 0) {
@@ -378,7 +442,7 @@ WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count) {
       if (static_cast<size_t>(L.total) + 1024 > 232448) continue;
       pl.splits = splits;
       pl.stages = stages;
-      pl.tmem_cols = pow2_at_least(((pl.mtile + 15) & ~15) + 4 * stages + 4 * nmax);
+      pl.tmem_cols = pow2_at_least(((pl.mtile + 15) & ~15) + 8 * stages);
       const int max_res = 512 / pl.tmem_cols;
       const size_t min_smem = 233472 / static_cast<size_t>(max_res + 1) + 1;
       pl.smem = std::max(static_cast<size_t>(L.total) + 1024, min_smem);

@@ -356,6 +356,27 @@ int pow2_at_least(int v) {
 
 }  // namespace
 
+// K-splits measured on a GB300 (152 SMs) for the projection shapes of the decode
+// step, as back-to-back launches under PDL with weights streamed from HBM: the
+// fastest split count per (N, K) and row range. Short K-ranges favour more CTAs
+// than SMs (two co-resident per SM); the long K=8192 range favours one deep
+// ring per SM. Shapes not listed use the SM-count rule in plan_gemm.
+struct SplitEntry {
+  int n, k, max_m, splits;
+};
+constexpr SplitEntry kSplitTable[] = {
+    {2048, 5120, 256, 8},                                       // fused_wqa_wkv (G1)
+    {8192, 1536, 4, 2},   {8192, 1536, 32, 4}, {8192, 1536, 256, 6},  // wq_b (G2)
+    {5120, 8192, 256, 3},                                       // third projection (G3)
+    {5120, 4096, 256, 6},                                       // wo_b
+};
+
+static int table_splits(int M, int N, int K) {
+  for (const SplitEntry& e : kSplitTable)
+    if (e.n == N && e.k == K && M <= e.max_m) return e.splits;
+  return 0;
+}
+
 GemmPlan plan_gemm(int M, int N, int K, int sm_count) {
   GemmPlan pl{};
   pl.mtile = (M + 15) & ~15;
@@ -363,6 +384,8 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count) {
   const int nchunks = K / 128;
   const int nsfb = (pl.mtile + 127) / 128;
   int splits = std::max(1, sm_count / std::max(tiles, 1));
+  // the table was measured with 152 SMs; other parts keep the SM-count rule
+  if (sm_count == 152 && table_splits(M, N, K) > 0) splits = table_splits(M, N, K);
   splits = std::min(splits, std::min(8, nchunks));
   if (const char* e = getenv("MX_SPLITS")) {
     const int v = atoi(e);

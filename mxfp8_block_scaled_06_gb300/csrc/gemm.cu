@@ -330,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  cluster_sync();
+  // the peers' reads of this CTA's partials have completed (their values were
+  // consumed), so ordering the exits needs no memory release
+  cluster_sync_relaxed();
 
   // ---------------- teardown
   if (*abort_flag != 0) {

@@ -251,6 +251,15 @@ def run_ours(args):
         us = ms * 1e3 / (5 * n_launch)
         gemm_us[m] = us
         gemm_gbs[m] = gemm_bytes(m, N1, K1) / (us * 1e-6) / 1e9
+    # the same step with the quantization inside the GEMM (mx_gemm_bf16: one
+    # launch per projection instead of two)
+    fused_us = {}
+    for m in M_LIST:
+        def fused(i, m=m):
+            wq, ws = wts[i % nset][0]
+            mx.mx_gemm_bf16(h, xs[m], wq, ws, out=outs[m], pdl=True, stream=stream)
+        ms, _ = time_graph(torch, fused, 5, 400, stream)
+        fused_us[m] = ms * 1e3 / (5 * 400)
     # dominant kernel: mx_gemm over the step's mix of M
     ms, _ = time_graph(torch, lambda i: step(i, quant=False), 5, 100, stream)
     gemm_launch_us = ms * 1e3 / (5 * 100 * len(M_LIST))
@@ -393,6 +402,7 @@ def run_ours(args):
         "gemm_gbs": {str(m): round(v, 1) for m, v in gemm_gbs.items()},
         "gemm_frac_of_peak": {str(m): round(v / pk["hbm_gbs"], 3) for m, v in gemm_gbs.items()},
         "quantize_us": {str(m): round(v, 3) for m, v in quant_us.items()},
+        "quantize_plus_gemm_fused_us": {str(m): round(v, 3) for m, v in fused_us.items()},
         "chain_us_per_step": chain, "wo_a": woa, "sweep": sweep,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": k_eff * 2 * len(M_LIST), "clocks": clk, "device_status": status,

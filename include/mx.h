@@ -103,6 +103,24 @@ int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scal
             const void* w, const void* w_scales, void* out, unsigned flags,
             void* stream);
 
+/* mx_gemm with bf16 activations quantized inside the GEMM: out equals, bit for
+ * bit, mx_quantize_rows(x) (swizzled scales) followed by mx_gemm on the same
+ * stream (the mxfp8 page's `wide_mm` / `pinned_mm` quantize the bf16 x and
+ * then run the MXFP8 GEMM: two launches; here one). Each CTA quantizes the
+ * K-range it contracts, in shared memory; the MXFP8 activation is not written.
+ *   x        [M, K] bf16, row stride ldx elements (ldx >= K, ldx % 8 == 0),
+ *            16-byte aligned.
+ *   w, w_scales, out, flags: as in mx_gemm.
+ * Constraints: as mx_gemm; MX_ERR_UNSUPPORTED also when the K-range's
+ * quantized rows do not fit in one CTA's shared memory (large M with few
+ * K-splits): the caller then uses mx_quantize_rows + mx_gemm.
+ * Cost: every CTA quantizes the K-range it contracts, so the N/128 weight
+ * tiles repeat that work; it saves a launch and wins at one or two rows, while
+ * from about four rows on the two-launch path is faster (measured on GB300). */
+int mx_gemm_bf16(mx_handle* h, int M, int N, int K, const void* x, long ldx,
+                 const void* w, const void* w_scales, void* out, unsigned flags,
+                 void* stream);
+
 /* The three projections of a decode step's attention on one stream
  * (fused_wqa_wkv -> wq_b -> wo_b on the mxfp8 page and in `AttentionStep.run`
  * of the page "...specialized_decode.attention.step"), every kernel launched

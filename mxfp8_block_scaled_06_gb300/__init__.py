@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libmx.so")
 MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_DEVICE, MX_ERR_CUDA, MX_ERR_TIMEOUT = range(6)
 MX_FLAG_PDL = 1
 
-EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows", "mx_gemm",
+EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows", "mx_gemm", "mx_gemm_bf16",
            "mx_gemm_chain", "wo_a_grouped", "mx_device_status", "mx_status_string"]
 
 _vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
@@ -52,6 +52,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx_scale_bytes.restype = ctypes.c_size_t
     lib.mx_quantize_rows.argtypes = [_vp, _i, _i, _vp, _l, _vp, _vp, _i, _vp]
     lib.mx_gemm.argtypes = [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _u, _vp]
+    lib.mx_gemm_bf16.argtypes = [_vp, _i, _i, _i, _vp, _l, _vp, _vp, _vp, _u, _vp]
     lib.mx_gemm_chain.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp]
     lib.wo_a_grouped.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i,
@@ -141,6 +142,21 @@ def mx_gemm(h: Handle, a, a_scales, w, w_scales, out=None, m: int | None = None,
         out = torch.empty((m, n), dtype=torch.bfloat16, device=w.device)
     _check(load_library().mx_gemm(h.ptr, m, n, k, _ptr(a), _ptr(a_scales), _ptr(w), _ptr(w_scales),
                                   _ptr(out), MX_FLAG_PDL if pdl else 0, _stream(stream)), "mx_gemm")
+    return out
+
+
+def mx_gemm_bf16(h: Handle, x, w, w_scales, out=None, m: int | None = None, pdl: bool = False,
+                 stream=None):
+    """out[M, N] bf16 = dequant(MXFP8(x[M, K])) x dequant(w[N, K])^T, x bf16 with its
+    quantization inside the GEMM kernel (row stride x.stride(0))."""
+    import torch
+    m = x.shape[0] if m is None else m
+    n, k = w.shape
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=w.device)
+    _check(load_library().mx_gemm_bf16(h.ptr, m, n, k, _ptr(x), x.stride(0), _ptr(w), _ptr(w_scales),
+                                       _ptr(out), MX_FLAG_PDL if pdl else 0, _stream(stream)),
+           "mx_gemm_bf16")
     return out
 
 

@@ -57,15 +57,21 @@ int validate_gemm(const mx_handle* h, int M, int N, int K, const void* a, const 
   return MX_OK;
 }
 
+// a = MXFP8 activations (+ a_scales), or x = bf16 activations with row stride
+// ldx (quantized inside the kernel); exactly one of the two is non-null
 int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
                 const void* w, const void* w_scales, void* out, uint8_t* q, uint8_t* q_scales,
-                int q_cols, bool pdl, cudaStream_t stream) {
-  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count);
+                int q_cols, bool pdl, cudaStream_t stream, const void* x = nullptr, long ldx = 0) {
+  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, x != nullptr);
   CUtensorMap tm_w, tm_a;
   int rc = make_tmap(h, &tm_w, w, N, K, 128);
   if (rc != MX_OK) return rc;
-  rc = make_tmap(h, &tm_a, a, M, K, plan.mtile);
-  if (rc != MX_OK) return rc;
+  if (x != nullptr) {
+    tm_a = tm_w;  // not read by the fused kernel
+  } else {
+    rc = make_tmap(h, &tm_a, a, M, K, plan.mtile);
+    if (rc != MX_OK) return rc;
+  }
   mx::GemmArgs args = {};
   args.M = M;
   args.N = N;
@@ -76,6 +82,8 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
   args.tmem_cols = plan.tmem_cols;
   args.a_scales = static_cast<const uint8_t*>(a_scales);
   args.w_scales = static_cast<const uint8_t*>(w_scales);
+  args.x = static_cast<const uint16_t*>(x);
+  args.ldx = ldx;
   args.out = out;
   args.q = q;
   args.q_scales = q_scales;
@@ -174,6 +182,22 @@ int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scal
   if (flags & ~MX_FLAG_PDL) return MX_ERR_INVALID_ARG;
   return gemm_launch(h, M, N, K, a, a_scales, w, w_scales, out, nullptr, nullptr, 0,
                      (flags & MX_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream));
+}
+
+int mx_gemm_bf16(mx_handle* h, int M, int N, int K, const void* x, long ldx, const void* w,
+                 const void* w_scales, void* out, unsigned flags, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (M < 1 || N < 1 || K < 1 || x == nullptr || w == nullptr || w_scales == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(w_scales, 32)) return MX_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldx < K || ldx % 8 != 0) return MX_ERR_INVALID_ARG;
+  if (out == nullptr || !aligned(out, 16)) return MX_ERR_INVALID_ARG;
+  if (flags & ~MX_FLAG_PDL) return MX_ERR_INVALID_ARG;
+  if (M > 256 || N % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
+  if (mx::plan_gemm(M, N, K, h->sm_count, true).smem > mx::kMaxDynamicSmem) return MX_ERR_UNSUPPORTED;
+  return gemm_launch(h, M, N, K, nullptr, nullptr, w, w_scales, out, nullptr, nullptr, 0,
+                     (flags & MX_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream), x, ldx);
 }
 
 int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, const mx_weight w[3],

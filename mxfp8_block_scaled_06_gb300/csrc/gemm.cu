@@ -41,20 +41,26 @@ constexpr uint32_t kSfTileBytes = 512;       // one 128x4 scale tile
 
 // Shared-memory carve-up of one CTA: a ring of `stages` (weight box, activation
 // box) pairs, then the weight and activation scale tiles of the CTA's whole
-// K-range (loaded once), then the mbarriers.
+// K-range (loaded once), then the mbarriers. With bf16 activations quantized in
+// the kernel (`fused`), the ring holds weight boxes only and the activation
+// tiles of the whole K-range are resident, after the scale tiles, followed by a
+// staging area for up to kRowBatch bf16 rows of the K-range.
+constexpr int kRowBatch = 32;
 struct Layout {
-  uint32_t a_bytes, stage_bytes, ring_bytes, sfa_bytes, sfb_bytes, bars;
+  uint32_t a_bytes, stage_bytes, ring_bytes, sfa_bytes, sfb_bytes, act, xraw, bars;
   int stages, nsfb, nmax;
-  __host__ __device__ Layout(int mtile, int stages_, int nmax_) {
+  __host__ __device__ Layout(int mtile, int stages_, int nmax_, bool fused = false, int xrows = 0) {
     stages = stages_;
     nmax = nmax_;
     nsfb = (mtile + 127) / 128;
     a_bytes = static_cast<uint32_t>(mtile) * 128u;
-    stage_bytes = (kWTileBytes + a_bytes + 1023u) & ~1023u;
+    stage_bytes = fused ? kWTileBytes : (kWTileBytes + a_bytes + 1023u) & ~1023u;
     ring_bytes = static_cast<uint32_t>(stages) * stage_bytes;
     sfa_bytes = static_cast<uint32_t>(nmax) * kSfTileBytes;
     sfb_bytes = static_cast<uint32_t>(nmax * nsfb) * kSfTileBytes;
-    bars = ring_bytes + sfa_bytes + sfb_bytes;
+    act = (ring_bytes + sfa_bytes + sfb_bytes + 1023u) & ~1023u;
+    xraw = act + (fused ? static_cast<uint32_t>(nmax) * a_bytes : 0u);
+    bars = xraw + (fused ? static_cast<uint32_t>(xrows * nmax) * 256u : 0u);
   }
   __host__ __device__ uint32_t w_off(int s) const { return s * stage_bytes; }
   __host__ __device__ uint32_t a_off(int s) const { return s * stage_bytes + kWTileBytes; }
@@ -62,14 +68,14 @@ struct Layout {
   __host__ __device__ uint32_t sfb_off(int rt, int i) const {
     return ring_bytes + sfa_bytes + (rt * nmax + i) * kSfTileBytes;
   }
-  // full[stages], empty[stages], sfa, sfb, accum; then TMEM slot and abort flag
-  __host__ __device__ uint32_t bar_bytes() const { return 8u * (2 * stages + 3) + 16u; }
+  // full[stages], empty[stages], sfa, sfb, accum, x; then TMEM slot and abort flag
+  __host__ __device__ uint32_t bar_bytes() const { return 8u * (2 * stages + 4) + 16u; }
   __host__ __device__ size_t total() const { return 1024 + bars + bar_bytes(); }
 };
 
 __host__ __device__ inline int tmem_sfa_col(int mtile) { return (mtile + 15) & ~15; }
 
-template <bool kRequant>
+template <bool kRequant, bool kFusedA>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                 const GemmArgs p) {
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c_begin = split * p.nchunks / S;
   const int n = (split + 1) * p.nchunks / S - c_begin;
   const int stages = p.stages;
-  const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S);
+  const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S, kFusedA, min(p.M, kRowBatch));
   const int nsfb = L.nsfb;
 
   const uint32_t bars = base + L.bars;
@@ -97,21 +103,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sfa_bar = bars + 16u * stages;
   const uint32_t sfb_bar = sfa_bar + 8u;
   const uint32_t accum_bar = sfa_bar + 16u;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L.bars + 8 * (2 * stages + 3));
+  const uint32_t x_bar = sfa_bar + 24u;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L.bars + 8 * (2 * stages + 4));
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(full(s), 2);
+      mbar_init(full(s), kFusedA ? 1 : 2);
       mbar_init(empty(s), 1);
     }
     mbar_init(sfa_bar, 1);
     mbar_init(sfb_bar, 1);
     mbar_init(accum_bar, 1);
+    mbar_init(x_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w);
-    prefetch_tmap(&tm_a);
+    if (!kFusedA) prefetch_tmap(&tm_a);
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
   tc_fence_before();
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_a = policy_evict_last();
   const bool w_lane = warp == 0 && lane < stages;
-  const bool a_lane = warp == 3 && lane < stages;
+  const bool a_lane = !kFusedA && warp == 3 && lane < stages;
   int last = -1;      // last chunk this lane loaded (weight or activation warps)
   int issued_n = 0;   // chunks its warp has loaded so far (warp-uniform)
   auto issue_w = [&](int i, int s) {
@@ -160,14 +168,100 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
 
   // ---------------- activations (written by the previous kernel on the stream)
-  if (a_lane && lane < n) issue_a(lane, lane);
-  if (warp == 3) issued_n = min(n, stages);
-  if (warp == 2 && lane == 1) {
-    mbar_expect_tx(sfb_bar, static_cast<uint32_t>(n * nsfb) * kSfTileBytes);
-    for (int rt = 0; rt < nsfb; ++rt)
-      bulk_load(base + L.sfb_off(rt, 0),
-                p.a_scales + (static_cast<size_t>(rt) * p.nchunks + c_begin) * kSfTileBytes,
-                static_cast<uint32_t>(n) * kSfTileBytes, sfb_bar, pol_a);
+  int x_batches = 0;  // bf16 row batches requested (fused), warp 3
+  if constexpr (!kFusedA) {
+    if (a_lane && lane < n) issue_a(lane, lane);
+    if (warp == 3) issued_n = min(n, stages);
+    if (warp == 2 && lane == 1) {
+      mbar_expect_tx(sfb_bar, static_cast<uint32_t>(n * nsfb) * kSfTileBytes);
+      for (int rt = 0; rt < nsfb; ++rt)
+        bulk_load(base + L.sfb_off(rt, 0),
+                  p.a_scales + (static_cast<size_t>(rt) * p.nchunks + c_begin) * kSfTileBytes,
+                  static_cast<uint32_t>(n) * kSfTileBytes, sfb_bar, pol_a);
+    }
+  } else {
+    // bf16 rows of the CTA's K-range -> MXFP8 codes in the 128-byte-swizzled
+    // K-major operand layout and the 128x4 scale tiles, in shared memory
+    const uint32_t at = L.a_bytes;
+    for (int idx = threadIdx.x; idx < n * (p.mtile - p.M) * 8; idx += kThreads) {
+      // zero rows [M, mtile) of every chunk tile
+      const int i = idx / ((p.mtile - p.M) * 8), rem = idx % ((p.mtile - p.M) * 8);
+      const int m = p.M + rem / 8;
+      *reinterpret_cast<uint4*>(base_ptr + L.act + i * at + m * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    for (int idx = threadIdx.x; idx < n * nsfb * 32; idx += kThreads)
+      *reinterpret_cast<uint4*>(base_ptr + L.sfb_off(idx / (n * 32), 0) + (idx % (n * 32)) * 16) =
+          make_uint4(0, 0, 0, 0);
+    const int units_per_row = n * 16;  // 8-element units in the K-range
+    for (int r0 = 0, batch = 0; r0 < p.M; r0 += kRowBatch, ++batch) {
+      const int rb = min(kRowBatch, p.M - r0);
+      if (warp == 3) {
+        // one lane per row: each row's K-range is contiguous
+        if (lane == 0) mbar_expect_tx(x_bar, static_cast<uint32_t>(rb * n) * 256u);
+        __syncwarp();
+        if (lane < rb)
+          bulk_load(base + L.xraw + lane * L.nmax * 256,
+                    p.x + static_cast<size_t>(r0 + lane) * p.ldx + static_cast<size_t>(c_begin) * 128,
+                    static_cast<uint32_t>(n) * 256u, x_bar, pol_a);
+        x_batches = batch + 1;
+      }
+      if (!mbar_wait(x_bar, batch & 1)) fail();
+      const int total = rb * units_per_row;
+      for (int b0 = 0; b0 < total; b0 += kThreads) {
+        const int u = b0 + threadIdx.x;
+        const bool valid = u < total && *abort_flag == 0;
+        const int row = u / units_per_row;
+        const int ul = u % units_per_row;
+        const int blk = ul >> 2;  // 32-block within the K-range
+        float v[8];
+        float amax = 0.f;
+        uint32_t nonfinite = 0;
+        if (valid) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(base_ptr + L.xraw + row * L.nmax * 256 + ul * 16);
+          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[2 * e] = __uint_as_float(w4[e] << 16);
+            v[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            amax = fmaxf(amax, fabsf(v[e]));
+            nonfinite |= !isfinite(v[e]);
+          }
+        }
+        // the four units of a 32-block sit in four consecutive lanes
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 1);
+        nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 2);
+        if (valid) {
+          uint32_t sbyte, lo, hi;
+          if (nonfinite) {
+            sbyte = 0xFFu;
+            lo = hi = 0x7F7F7F7Fu;
+          } else {
+            sbyte = mx_scale_byte(amax);
+            const float f = mx_inv_scale(sbyte);
+            lo = cvt_e4m3x2(v[0] * f, v[1] * f) | (cvt_e4m3x2(v[2] * f, v[3] * f) << 16);
+            hi = cvt_e4m3x2(v[4] * f, v[5] * f) | (cvt_e4m3x2(v[6] * f, v[7] * f) << 16);
+          }
+          const int m = r0 + row;
+          const int ci = blk >> 2;                       // chunk within the K-range
+          const int kb = (blk & 3) * 32 + (ul & 3) * 8;  // byte within the 128-byte row
+          const uint32_t off = ci * at + (m >> 3) * 1024 + (m & 7) * 128 +
+                               (((kb >> 4) ^ (m & 7)) << 4) + (kb & 15);
+          *reinterpret_cast<uint2*>(base_ptr + L.act + off) = make_uint2(lo, hi);
+          if ((ul & 3) == 0)
+            base_ptr[L.sfb_off(m >> 7, ci) + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (blk & 3)] =
+                static_cast<uint8_t>(sbyte);
+        }
+      }
+      __syncthreads();  // the next batch reuses the staging rows
+    }
+    fence_proxy_async_smem();  // written by the threads, read by the tensor cores
+    __syncthreads();
   }
 
   if (warp == 0 || warp == 3) {
@@ -177,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool weights = warp == 0;
     int s = 0, issuer = stages & 31;
     uint32_t ph = 0, empty_s = empty(0);
-    for (int i = stages; i < n; ++i) {
+    for (int i = stages; i < (kFusedA && !weights ? 0 : n); ++i) {
       bool freed = mbar_try_wait(empty_s, ph);
       if (!__all_sync(0xFFFFFFFFu, freed)) freed = *abort_flag == 0 && mbar_wait(empty_s, ph);
       if (!__all_sync(0xFFFFFFFFu, freed)) {
@@ -207,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // field in 16-byte units) and stage, phase, barrier and TMEM addresses are
     // running values rather than divisions and products.
     const uint64_t wd = sdesc_k_sw128(base + L.w_off(0));
-    const uint64_t ad = sdesc_k_sw128(base + L.a_off(0));
+    const uint64_t ad = sdesc_k_sw128(base + (kFusedA ? L.act : L.a_off(0)));
     const uint64_t fd = sdesc_sf(base + L.sfa_off(0));
     const uint64_t gd = sdesc_sf(base + L.sfb_off(0, 0));
     const uint32_t op_hi = static_cast<uint32_t>(wd >> 32), sf_hi = static_cast<uint32_t>(fd >> 32);
@@ -217,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id2 = idesc_mxf8(p.mtile, 2), id3 = idesc_mxf8(p.mtile, 3);
     // every wait below is taken by all lanes and decided by a warp vote, so the
     // warp stays converged for elect.sync and leaves the loop together
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfa_bar, 0) && mbar_wait(sfb_bar, 0))) {
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfa_bar, 0) && (kFusedA || mbar_wait(sfb_bar, 0)))) {
       if (lane == 0) fail();
     } else {
       uint32_t w_lo = static_cast<uint32_t>(wd), a_lo = static_cast<uint32_t>(ad);
@@ -247,18 +341,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         f_lo += kSfTileBytes >> 4;
         g_lo += kSfTileBytes >> 4;
+        if (kFusedA) a_lo += L.a_bytes >> 4;  // resident tiles: one per chunk
         if (++s == stages) {
           s = 0;
           ph ^= 1u;
           w_lo = static_cast<uint32_t>(wd);
-          a_lo = static_cast<uint32_t>(ad);
+          if (!kFusedA) a_lo = static_cast<uint32_t>(ad);
           ta = tmem + sfa_col;
           tb = tmem + sfb_col;
           full_s = full(0);
           empty_s = empty(0);
         } else {
           w_lo += stage_units;
-          a_lo += stage_units;
+          if (!kFusedA) a_lo += stage_units;
           ta += 4;
           tb += 4 * nsfb;
           full_s += 8;
@@ -341,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // had landed before the stage was refilled)
     if (last >= 0 && last + stages >= issued_n) mbar_wait(full(last % stages), (last / stages) & 1);
     if (warp == 2 && lane == 0) mbar_wait(sfa_bar, 0);
-    if (warp == 2 && lane == 1) mbar_wait(sfb_bar, 0);
+    if (warp == 2 && lane == 1 && !kFusedA) mbar_wait(sfb_bar, 0);
+    if (warp == 3 && lane == 0 && x_batches > 0) mbar_wait(x_bar, (x_batches - 1) & 1);
   }
   __syncthreads();
   if (warp == 0) {
@@ -379,7 +475,7 @@ static int table_splits(int M, int N, int K) {
   return 0;
 }
 
-GemmPlan plan_gemm(int M, int N, int K, int sm_count) {
+GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a) {
   GemmPlan pl{};
   pl.mtile = (M + 15) & ~15;
   const int tiles = N / 128;
@@ -400,8 +496,11 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count) {
   while (splits < std::min(8, nchunks) && scale_bytes(splits) > 48 * 1024) ++splits;
   pl.splits = splits;
   const int per_cta = (nchunks + splits - 1) / splits;
-  const Layout L1(pl.mtile, 1, per_cta);
-  const size_t scales = L1.sfa_bytes + L1.sfb_bytes;
+  const int xrows = std::min(M, kRowBatch);
+  const Layout L1(pl.mtile, 1, per_cta, fused_a, xrows);
+  // resident per CTA besides the ring: scale tiles (and, fused, the activation
+  // tiles and the bf16 staging rows)
+  const size_t scales = L1.bars - L1.ring_bytes;
   // Short K-ranges (all chunks in flight at once): about 100 KB per CTA, so the
   // next kernel's CTAs fit beside this one. Long ones: a deep ring (more bytes
   // in flight per SM) matters more than that overlap.
@@ -413,12 +512,12 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count) {
     if (v >= 1 && v <= 12) stages = v;
   }
   stages = std::min(stages, per_cta);
-  // the epilogue stages the fp32 partials [mtile][128] over the ring and scale tiles
+  // the epilogue stages the fp32 partials [mtile][128] over the ring and what follows it
   while (static_cast<size_t>(stages) * L1.stage_bytes + scales < static_cast<size_t>(pl.mtile) * 512)
     ++stages;
   pl.stages = stages;
   pl.tmem_cols = pow2_at_least(tmem_sfa_col(pl.mtile) + 4 * stages * (1 + nsfb));
-  const Layout L(pl.mtile, stages, per_cta);
+  const Layout L(pl.mtile, stages, per_cta, fused_a, xrows);
   // CTAs that can share an SM must fit their TMEM together: ask for enough
   // shared memory that at most 512 / tmem_cols of them are resident.
   const int max_res = 512 / pl.tmem_cols;
@@ -428,8 +527,10 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count) {
 }
 
 cudaError_t set_gemm_attributes() {
-  const void* ks[2] = {reinterpret_cast<const void*>(&gemm_kernel<false>),
-                       reinterpret_cast<const void*>(&gemm_kernel<true>)};
+  const void* ks[4] = {reinterpret_cast<const void*>(&gemm_kernel<false, false>),
+                       reinterpret_cast<const void*>(&gemm_kernel<true, false>),
+                       reinterpret_cast<const void*>(&gemm_kernel<false, true>),
+                       reinterpret_cast<const void*>(&gemm_kernel<true, true>)};
   for (const void* k : ks) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMaxDynamicSmem));
@@ -460,8 +561,12 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const 
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  if (args.q != nullptr) return cudaLaunchKernelEx(&cfg, gemm_kernel<true>, tm_w, tm_a, args);
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<false>, tm_w, tm_a, args);
+  if (args.x != nullptr) {
+    if (args.q != nullptr) return cudaLaunchKernelEx(&cfg, gemm_kernel<true, true>, tm_w, tm_a, args);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<false, true>, tm_w, tm_a, args);
+  }
+  if (args.q != nullptr) return cudaLaunchKernelEx(&cfg, gemm_kernel<true, false>, tm_w, tm_a, args);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<false, false>, tm_w, tm_a, args);
 }
 
 }  // namespace mx

@@ -28,8 +28,12 @@ struct GemmPlan {
 struct GemmArgs {
   int M, N, K;
   int mtile, stages, nchunks, tmem_cols;
-  const uint8_t* a_scales;
+  const uint8_t* a_scales;  // MXFP8 activations' swizzled scales (unused when x is set)
   const uint8_t* w_scales;
+  // bf16 activations [M, K] (row stride ldx elements) quantized inside the
+  // kernel instead of MXFP8 activations through tm_a / a_scales; null = MXFP8 in
+  const uint16_t* x;
+  long ldx;
   void* out;          // bf16 [M, N] or null
   uint8_t* q;         // fused requantization of columns [0, q_cols): E4M3 [M, q_cols]
   uint8_t* q_scales;  // swizzled scales of q
@@ -37,7 +41,7 @@ struct GemmArgs {
   int* status;
 };
 
-GemmPlan plan_gemm(int M, int N, int K, int sm_count);
+GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a = false);
 cudaError_t set_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& args,
                         const GemmPlan& plan, bool pdl, cudaStream_t stream);

@@ -318,13 +318,22 @@ def run_ours(args):
                 run_woa(i)
                 wq, ws = ww[i % wset][1]
                 mx.mx_gemm(h, q, qs, wq, ws, out=ob, pdl=True, stream=stream)
+            xq = torch.empty((t, G * H * D), dtype=torch.uint8, device=rig.dev)
+            xqs = torch.empty(mx.mx_scale_bytes(t, G * H * D), dtype=torch.uint8, device=rig.dev)
+
+            def run_unfused(i, t=t, x=x, pos=pos, q=q, qs=qs, xq=xq, xqs=xqs):
+                wq, ws = ww[i % wset][0]
+                mx.wo_a_grouped_unfused(h, x, pos, cs, wq, ws, G, H, R, q=q, q_scales=qs, xq=xq,
+                                        xq_scales=xqs, stream=stream)
             ms_a, _ = time_graph(torch, run_woa, 5, 60, stream)
             ms_p, _ = time_graph(torch, run_pair, 5, 60, stream)
-            ua, up = ms_a * 1e3 / 300, ms_p * 1e3 / 300
+            ms_u, _ = time_graph(torch, run_unfused, 5, 60, stream)
+            ua, up, uu = ms_a * 1e3 / 300, ms_p * 1e3 / 300, ms_u * 1e3 / 300
             wa = w_bytes(*pair[0])
             woa[t] = {"wo_a_us": round(ua, 3), "wo_a_weight_gbs": round(wa / (ua * 1e-6) / 1e9, 1),
                       "wo_a_plus_wo_b_us": round(up, 3),
-                      "pair_weight_gbs": round((wa + w_bytes(*WOB)) / (up * 1e-6) / 1e9, 1)}
+                      "pair_weight_gbs": round((wa + w_bytes(*WOB)) / (up * 1e-6) / 1e9, 1),
+                      "wo_a_unfused_us": round(uu, 3)}
 
     # --------------------------------------------------------------- sweep
     sweep = {}

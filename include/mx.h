@@ -169,6 +169,28 @@ int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* po
                  void* debug_z, void* debug_xq, void* debug_xs, int early_trigger,
                  void* stream);
 
+/* The same projection as wo_a_grouped in two launches, for token counts the
+ * fused kernel does not take (the o_proj page's fallback: `grouped_forward`
+ * when the tokens exceed the fused limit, z then fed to wo_b):
+ *   1. inverse RoPE + per-32 MX quantization of every head -> xq, xq_scales;
+ *   2. one grouped block-scaled GEMM: the R output rows of group g contract
+ *      the group's K-slice of xq; z rounded to bf16 and requantized to q.
+ *   xq         [T, G*H*D] E4M3 (caller-owned intermediate), 16-byte aligned.
+ *   xq_scales  mx_scale_bytes(T, G*H*D) bytes, swizzled, 16-byte aligned.
+ *   z          optional [T, G*R] bf16 (the pre-quantization output), or null.
+ *   other arguments as in wo_a_grouped (H is not limited to 8 here).
+ * q / q_scales equal mx_quantize_rows of bf16(z). On GB300 the fused kernel is
+ * faster up to about 16 tokens and this path from 32 on (T = 32: 10.3 vs
+ * 16.1 us; T = 128: 22 vs 76 us). Constraints: 1 <= T <= 256,
+ * d_nope = 448, d_rope = 64, R % 128 == 0, else MX_ERR_UNSUPPORTED. A position
+ * outside [0, max_pos) reads cache row 0 and is reported by mx_device_status,
+ * as in wo_a_grouped. */
+int wo_a_grouped_unfused(mx_handle* h, int T, const void* x, long ldx,
+                         const int64_t* positions, const float* cos_sin, int max_pos,
+                         const void* w, const void* w_scales, int G, int H, int d_nope,
+                         int d_rope, int R, void* xq, void* xq_scales, void* z, void* q,
+                         void* q_scales, void* stream);
+
 /* Read and clear the device status word: MX_OK, or MX_ERR_TIMEOUT if a kernel
  * gave up on a bounded wait since the last call. Synchronizes the device. */
 int mx_device_status(mx_handle* h, int* status);

@@ -20,7 +20,8 @@ MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_DEVICE, MX_ERR_CUDA, MX_ER
 MX_FLAG_PDL = 1
 
 EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows", "mx_gemm", "mx_gemm_bf16",
-           "mx_gemm_chain", "wo_a_grouped", "mx_device_status", "mx_status_string"]
+           "mx_gemm_chain", "wo_a_grouped", "wo_a_grouped_unfused", "mx_device_status",
+           "mx_status_string"]
 
 _vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
 
@@ -57,6 +58,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                   _vp, _vp, _vp, _vp, _vp]
     lib.wo_a_grouped.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i,
                                  _vp, _vp, _vp, _vp, _vp, _i, _vp]
+    lib.wo_a_grouped_unfused.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i,
+                                         _i, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.mx_device_status.argtypes = [_vp, ctypes.POINTER(_i)]
     lib.mx_status_string.argtypes = [_i]
     lib.mx_status_string.restype = ctypes.c_char_p
@@ -205,6 +208,31 @@ def wo_a_grouped(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,
                                        _ptr(q), _ptr(q_scales), _ptr(dz), _ptr(dxq), _ptr(dxs),
                                        int(early_trigger), _stream(stream)), "wo_a_grouped")
     return dict(q=q, q_scales=q_scales, z=dz, xq=dxq, xs=dxs)
+
+
+def wo_a_grouped_unfused(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,
+                         heads_per_group: int, o_lora_rank: int, d_nope: int = 448,
+                         d_rope: int = 64, q=None, q_scales=None, xq=None, xq_scales=None,
+                         z: bool = False, stream=None) -> dict:
+    """wo_a_grouped in two launches (RoPE + quantize into the caller-owned xq, then a
+    grouped GEMM with the requantization fused); for token counts up to 256."""
+    import torch
+    t = x.shape[0]
+    dev = x.device
+    cols = n_groups * o_lora_rank
+    kall = n_groups * heads_per_group * (d_nope + d_rope)
+    q = _empty_u8((t, cols), dev) if q is None else q
+    q_scales = _empty_u8((mx_scale_bytes(t, cols),), dev) if q_scales is None else q_scales
+    xq = _empty_u8((t, kall), dev) if xq is None else xq
+    xq_scales = _empty_u8((mx_scale_bytes(t, kall),), dev) if xq_scales is None else xq_scales
+    zt = torch.empty((t, cols), dtype=torch.bfloat16, device=dev) if z else None
+    _check(load_library().wo_a_grouped_unfused(h.ptr, t, _ptr(x), x.stride(0), _ptr(positions),
+                                               _ptr(cos_sin), cos_sin.shape[0], _ptr(w),
+                                               _ptr(w_scales), n_groups, heads_per_group, d_nope,
+                                               d_rope, o_lora_rank, _ptr(xq), _ptr(xq_scales),
+                                               _ptr(zt), _ptr(q), _ptr(q_scales), _stream(stream)),
+           "wo_a_grouped_unfused")
+    return dict(q=q, q_scales=q_scales, z=zt, xq=xq, xq_scales=xq_scales)
 
 
 def mx_device_status(h: Handle) -> int:

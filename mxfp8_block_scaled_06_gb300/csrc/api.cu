@@ -31,7 +31,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 
 // 2-D uint8 tensor map over a row-major [rows, k] matrix, box {128 bytes, box_rows}
 // with the 128-byte swizzle; out-of-range rows of a box read as zero.
-int make_tmap(const mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, int k,
+int make_tmap(const mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, long k,
               int box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
@@ -58,10 +58,13 @@ int validate_gemm(const mx_handle* h, int M, int N, int K, const void* a, const 
 }
 
 // a = MXFP8 activations (+ a_scales), or x = bf16 activations with row stride
-// ldx (quantized inside the kernel); exactly one of the two is non-null
+// ldx (quantized inside the kernel); exactly one of the two is non-null.
+// groups > 1: a is [M, groups * K] and the weight tiles of group g (N / groups
+// rows each) contract its K-slice g.
 int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
                 const void* w, const void* w_scales, void* out, uint8_t* q, uint8_t* q_scales,
-                int q_cols, bool pdl, cudaStream_t stream, const void* x = nullptr, long ldx = 0) {
+                int q_cols, bool pdl, cudaStream_t stream, const void* x = nullptr, long ldx = 0,
+                int groups = 1) {
   const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, x != nullptr);
   CUtensorMap tm_w, tm_a;
   int rc = make_tmap(h, &tm_w, w, N, K, 128);
@@ -69,7 +72,7 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
   if (x != nullptr) {
     tm_a = tm_w;  // not read by the fused kernel
   } else {
-    rc = make_tmap(h, &tm_a, a, M, K, plan.mtile);
+    rc = make_tmap(h, &tm_a, a, M, static_cast<long>(K) * groups, plan.mtile);
     if (rc != MX_OK) return rc;
   }
   mx::GemmArgs args = {};
@@ -84,6 +87,8 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
   args.w_scales = static_cast<const uint8_t*>(w_scales);
   args.x = static_cast<const uint16_t*>(x);
   args.ldx = ldx;
+  args.group_tiles = groups > 1 ? N / groups / 128 : 0;
+  args.a_sf_chunks = K / 128 * groups;
   args.out = out;
   args.q = q;
   args.q_scales = q_scales;
@@ -274,6 +279,38 @@ int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* po
   args.early_trigger = early_trigger;
   args.status = h->d_status;
   return cuda_status(mx::launch_wo_a(tm_w, args, plan, static_cast<cudaStream_t>(stream)));
+}
+
+int wo_a_grouped_unfused(mx_handle* h, int T, const void* x, long ldx, const int64_t* positions,
+                         const float* cos_sin, int max_pos, const void* w, const void* w_scales,
+                         int G, int H, int d_nope, int d_rope, int R, void* xq, void* xq_scales,
+                         void* z, void* q, void* q_scales, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (x == nullptr || positions == nullptr || cos_sin == nullptr || w == nullptr ||
+      w_scales == nullptr || xq == nullptr || xq_scales == nullptr || q == nullptr ||
+      q_scales == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (T < 1 || G < 1 || H < 1 || R < 1 || max_pos < 1) return MX_ERR_INVALID_ARG;
+  if (d_nope != 448 || d_rope != 64 || R % 128 != 0 || T > 256) return MX_ERR_UNSUPPORTED;
+  const int D = d_nope + d_rope;
+  const long kx = static_cast<long>(G) * H * D;  // the activation's K (all groups)
+  if (ldx < kx || ldx % 8 != 0) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(w_scales, 32) || !aligned(xq, 16) ||
+      !aligned(xq_scales, 16) || !aligned(q, 16) || !aligned(q_scales, 16) ||
+      !aligned(cos_sin, 16) || !aligned(positions, 8) || (z && !aligned(z, 16)))
+    return MX_ERR_INVALID_ARG;
+  if (kx > (1L << 30) || mx::plan_gemm(T, G * R, H * D, h->sm_count).smem > mx::kMaxDynamicSmem)
+    return MX_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // 1. inverse RoPE + MX quantize of all heads -> xq (swizzled scales over G*H*D)
+  const mx::RopeArgs rope{positions, cos_sin, max_pos, D, d_nope, h->d_status};
+  rc = cuda_status(mx::launch_quantize_rows(x, ldx, T, static_cast<int>(kx), xq, xq_scales, 1, s, rope));
+  if (rc != MX_OK) return rc;
+  // 2. one grouped GEMM: tile rows of group g contract xq's K-slice g; z rounded
+  //    to bf16 and requantized in the epilogue
+  return gemm_launch(h, T, G * R, H * D, xq, xq_scales, w, w_scales, z, static_cast<uint8_t*>(q),
+                     static_cast<uint8_t*>(q_scales), G * R, true, s, nullptr, 0, G);
 }
 
 int mx_device_status(mx_handle* h, int* status) {

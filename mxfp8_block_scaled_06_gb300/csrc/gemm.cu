@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c_begin = split * p.nchunks / S;
   const int n = (split + 1) * p.nchunks / S - c_begin;
   const int stages = p.stages;
+  // grouped activations: this tile's group reads its own K-slice of A
+  const int a_k0 = p.group_tiles > 0 ? (tile / p.group_tiles) * p.K : 0;
   const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S, kFusedA, min(p.M, kRowBatch));
   const int nsfb = L.nsfb;
 
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto issue_a = [&](int i, int s) {
     mbar_expect_tx(full(s), L.a_bytes);
-    tma_load_2d(base + L.a_off(s), &tm_a, full(s), (c_begin + i) * 128, 0, pol_a);
+    tma_load_2d(base + L.a_off(s), &tm_a, full(s), a_k0 + (c_begin + i) * 128, 0, pol_a);
     last = i;
   };
 
@@ -176,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(sfb_bar, static_cast<uint32_t>(n * nsfb) * kSfTileBytes);
       for (int rt = 0; rt < nsfb; ++rt)
         bulk_load(base + L.sfb_off(rt, 0),
-                  p.a_scales + (static_cast<size_t>(rt) * p.nchunks + c_begin) * kSfTileBytes,
+                  p.a_scales + (static_cast<size_t>(rt) * p.a_sf_chunks + a_k0 / 128 + c_begin) *
+                                   kSfTileBytes,
                   static_cast<uint32_t>(n) * kSfTileBytes, sfb_bar, pol_a);
     }
   } else {

@@ -11,8 +11,17 @@ namespace mx {
 constexpr size_t kMaxDynamicSmem = 232448;
 
 // ------------------------------------------------------------ quantizer
+// Inverse RoPE applied before quantizing (WO-A activation): rows are tokens of
+// heads of head_dim, dims from d_nope on rotated by -pos * f; cos_sin null = none.
+struct RopeArgs {
+  const int64_t* positions;
+  const float* cos_sin;  // [max_pos, 64]: 32 cos | 32 sin
+  int max_pos, head_dim, d_nope;
+  int* status;
+};
 cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q, void* scales,
-                                 int swizzled, cudaStream_t stream);
+                                 int swizzled, cudaStream_t stream,
+                                 const RopeArgs& rope = RopeArgs{nullptr, nullptr, 0, 0, 0, nullptr});
 
 // ------------------------------------------------------------ block-scaled GEMM
 // Plan of one GEMM launch: activation tile (MMA N), K-splits per weight tile
@@ -34,6 +43,12 @@ struct GemmArgs {
   // kernel instead of MXFP8 activations through tm_a / a_scales; null = MXFP8 in
   const uint16_t* x;
   long ldx;
+  // Grouped activations (0 = not grouped): weight tile t belongs to group
+  // g = t / group_tiles and contracts the group's K-slice [g K, (g + 1) K) of
+  // a wider MXFP8 activation whose scale layout has a_sf_chunks 128-wide
+  // column blocks per row tile (= K / 128 when not grouped).
+  int group_tiles;
+  int a_sf_chunks;
   void* out;          // bf16 [M, N] or null
   uint8_t* q;         // fused requantization of columns [0, q_cols): E4M3 [M, q_cols]
   uint8_t* q_scales;  // swizzled scales of q

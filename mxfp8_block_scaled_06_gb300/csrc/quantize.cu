@@ -6,6 +6,12 @@
 // warp, stores 256 bytes. Padding of the swizzled scale buffer (rows up to a
 // multiple of 128, block columns up to a multiple of 4) is written as zero by
 // the same grid so the whole buffer is defined.
+//
+// Optionally (rope != null) the rows are attention heads of `head_dim` whose
+// last dims from `d_nope` on are rotated first, the inverse RoPE of the WO-A
+// projection: adjacent pairs (a, b) at rope dim 2i become (a c + b s, b c - a s)
+// with c, s = the float32 cos/sin of the row's position (cache row [32 cos |
+// 32 sin]), each product and sum rounded to float32 (no fused multiply-add).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -19,7 +25,7 @@ constexpr int kWarpsPerBlock = 8;
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     quantize_rows_kernel(const uint16_t* __restrict__ x, long ldx, int M, int K,
                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales, int swizzled,
-                         int rows_total, int groups_per_row) {
+                         int rows_total, int groups_per_row, RopeArgs rope) {
   // Programmatic dependent launch: let the next kernel (typically a GEMM that
   // streams its weights first) start now; wait for the previous kernel before
   // touching memory it may produce or read.
@@ -47,10 +53,29 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     for (int i = 0; i < 4; ++i) {
       v[2 * i] = __uint_as_float(w[i] << 16);
       v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      nonfinite |= ((w[i] & 0x7F80u) == 0x7F80u) | ((w[i] & 0x7F800000u) == 0x7F800000u);
+    }
+    const int d = (blk * 32 + sub * 8) % (rope.cos_sin != nullptr ? rope.head_dim : 1);
+    if (rope.cos_sin != nullptr && d >= rope.d_nope) {
+      long long pos = rope.positions[row];
+      if (pos < 0 || pos >= rope.max_pos) {
+        atomicOr(rope.status, kStatusBadInput);  // position outside the cache: row 0
+        pos = 0;
+      }
+      const float* cs = rope.cos_sin + static_cast<size_t>(pos) * 64;
+      const int p0 = (d - rope.d_nope) >> 1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float c = cs[p0 + i], sn = cs[32 + p0 + i];
+        const float a = v[2 * i], b = v[2 * i + 1];
+        v[2 * i] = __fadd_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+        v[2 * i + 1] = __fsub_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
+      }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < 8; ++i) {
+      amax = fmaxf(amax, fabsf(v[i]));
+      nonfinite |= !isfinite(v[i]);
+    }
   }
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
@@ -84,7 +109,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 }  // namespace
 
 cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q, void* scales,
-                                 int swizzled, cudaStream_t stream) {
+                                 int swizzled, cudaStream_t stream, const RopeArgs& rope) {
   const int nblk = K / 32;
   const int cols = swizzled ? ((nblk + 3) & ~3) : nblk;
   const int groups_per_row = (cols + 7) / 8;
@@ -102,7 +127,7 @@ cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q,
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, quantize_rows_kernel, static_cast<const uint16_t*>(x), ldx, M, K,
                             static_cast<uint8_t*>(q), static_cast<uint8_t*>(scales), swizzled,
-                            rows_total, groups_per_row);
+                            rows_total, groups_per_row, rope);
 }
 
 }  // namespace mx

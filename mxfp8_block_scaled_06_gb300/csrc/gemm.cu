@@ -459,17 +459,18 @@ int pow2_at_least(int v) {
 
 // K-splits measured on a GB300 (152 SMs) for the projection shapes of the decode
 // step, as back-to-back launches under PDL with weights streamed from HBM: the
-// fastest split count per (N, K) and row range. Short K-ranges favour more CTAs
-// than SMs (two co-resident per SM); the long K=8192 range favours one deep
-// ring per SM. Shapes not listed use the SM-count rule in plan_gemm.
+// fastest split count per (N, K) and row range. More CTAs than SMs (two or
+// three co-resident per SM, each with a shallower ring) beat one deep ring per
+// SM as long as the grid fits in one wave. Shapes not listed use the SM-count
+// rule in plan_gemm.
 struct SplitEntry {
   int n, k, max_m, splits;
 };
 constexpr SplitEntry kSplitTable[] = {
-    {2048, 5120, 256, 8},                                       // fused_wqa_wkv (G1)
-    {8192, 1536, 4, 2},   {8192, 1536, 32, 4}, {8192, 1536, 256, 6},  // wq_b (G2)
-    {5120, 8192, 256, 3},                                       // third projection (G3)
-    {5120, 4096, 256, 6},                                       // wo_b
+    {2048, 5120, 256, 8},                         // fused_wqa_wkv (G1)
+    {8192, 1536, 4, 2},   {8192, 1536, 256, 6},   // wq_b (G2)
+    {5120, 8192, 32, 8},  {5120, 8192, 256, 6},   // third projection (G3)
+    {5120, 4096, 32, 8},  {5120, 4096, 256, 6},   // wo_b
 };
 
 static int table_splits(int M, int N, int K) {
@@ -505,9 +506,11 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a) {
   // tiles and the bf16 staging rows)
   const size_t scales = L1.bars - L1.ring_bytes;
   // Short K-ranges (all chunks in flight at once): about 100 KB per CTA, so the
-  // next kernel's CTAs fit beside this one. Long ones: a deep ring (more bytes
-  // in flight per SM) matters more than that overlap.
-  const size_t budget = per_cta <= 8 ? 100 * 1024 : 180 * 1024;
+  // next kernel's CTAs fit beside this one. Long ones: as deep a ring as lets
+  // the whole grid be resident in one wave (CTAs per SM x shared memory).
+  const int per_sm = (tiles * splits + sm_count - 1) / std::max(sm_count, 1);
+  const size_t wave = per_sm <= 1 ? 180 * 1024 : 227 * 1024 / static_cast<size_t>(per_sm) - 4 * 1024;
+  const size_t budget = per_cta <= 8 ? std::min<size_t>(100 * 1024, wave) : wave;
   int stages = budget > scales ? static_cast<int>((budget - scales) / L1.stage_bytes) : 0;
   stages = std::max(2, std::min(stages, 10));
   if (const char* e = getenv("MX_STAGES")) {

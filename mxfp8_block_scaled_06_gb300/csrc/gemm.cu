@@ -491,7 +491,7 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a) {
   splits = std::min(splits, std::min(8, nchunks));
   if (const char* e = getenv("MX_SPLITS")) {
     const int v = atoi(e);
-    if (v >= 1 && v <= 8) splits = std::min(v, nchunks);
+    if (v >= 1 && v <= 16) splits = std::min(v, nchunks);
   }
   // the scale tiles of a CTA's K-range stay resident: at most 48 KB of them
   auto scale_bytes = [&](int sp) {
@@ -538,7 +538,10 @@ cudaError_t set_gemm_attributes() {
                        reinterpret_cast<const void*>(&gemm_kernel<false, true>),
                        reinterpret_cast<const void*>(&gemm_kernel<true, true>)};
   for (const void* k : ks) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // clusters of up to 16 K-splits (beyond the portable 8)
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMaxDynamicSmem));
     if (e != cudaSuccess) return e;
   }

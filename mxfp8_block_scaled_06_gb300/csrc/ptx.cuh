@@ -131,16 +131,19 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
-// Sum of the float at shared offset `addr` over cluster ranks 0..S-1 (S <= 8),
-// in rank order; all S loads are issued before the first add.
+// Sum of the float at shared offset `addr` over cluster ranks 0..S-1 (S <= 16),
+// in rank order; the loads of each group of 8 ranks are issued before their adds.
 __device__ __forceinline__ float cluster_sum(uint32_t addr, int S) {
-  float v[8];
-#pragma unroll
-  for (int r = 0; r < 8; ++r) v[r] = r < S ? ld_shared_cluster_f32(map_shared_rank(addr, r)) : 0.f;
   float acc = 0.f;
+  for (int r0 = 0; r0 < S; r0 += 8) {
+    float v[8];
 #pragma unroll
-  for (int r = 0; r < 8; ++r)
-    if (r < S) acc += v[r];
+    for (int r = 0; r < 8; ++r)
+      v[r] = r0 + r < S ? ld_shared_cluster_f32(map_shared_rank(addr, r0 + r)) : 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r0 + r < S) acc += v[r];
+  }
   return acc;
 }
 

@@ -541,6 +541,10 @@ cudaError_t set_gemm_attributes() {
     // clusters of up to 16 K-splits (beyond the portable 8)
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
+    // the whole unified L1/shared array as shared memory, so that every plan's
+    // CTAs-per-SM fit from the first launch on
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMaxDynamicSmem));
     if (e != cudaSuccess) return e;

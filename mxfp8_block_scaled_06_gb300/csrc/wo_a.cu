@@ -460,8 +460,10 @@ WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count) {
 }
 
 cudaError_t set_wo_a_attributes() {
-  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&wo_a_kernel),
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  const void* k = reinterpret_cast<const void*>(&wo_a_kernel);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
 }
 
 cudaError_t launch_wo_a(const CUtensorMap& tm_w, const WoaArgs& args, const WoaPlan& plan,

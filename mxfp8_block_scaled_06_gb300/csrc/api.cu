@@ -89,8 +89,6 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
   args.ldx = ldx;
   args.group_tiles = groups > 1 ? N / groups / 128 : 0;
   args.a_sf_chunks = K / 128 * groups;
-  args.w = static_cast<const uint8_t*>(w);
-  args.lsu_w = plan.lsu_w;
   args.out = out;
   args.q = q;
   args.q_scales = q_scales;

@@ -68,8 +68,8 @@ struct Layout {
   __host__ __device__ uint32_t sfb_off(int rt, int i) const {
     return ring_bytes + sfa_bytes + (rt * nmax + i) * kSfTileBytes;
   }
-  // full[stages], empty[stages], sfa, sfb, accum, x, w; then TMEM slot and abort flag
-  __host__ __device__ uint32_t bar_bytes() const { return 8u * (2 * stages + 5) + 16u; }
+  // full[stages], empty[stages], sfa, sfb, accum, x; then TMEM slot and abort flag
+  __host__ __device__ uint32_t bar_bytes() const { return 8u * (2 * stages + 4) + 16u; }
   __host__ __device__ size_t total() const { return 1024 + bars + bar_bytes(); }
 };
 
@@ -106,8 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sfb_bar = sfa_bar + 8u;
   const uint32_t accum_bar = sfa_bar + 16u;
   const uint32_t x_bar = sfa_bar + 24u;
-  const uint32_t w_bar = sfa_bar + 32u;  // load/store-path weights landed (every thread arrives)
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L.bars + 8 * (2 * stages + 5));
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L.bars + 8 * (2 * stages + 4));
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
@@ -119,7 +118,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sfb_bar, 1);
     mbar_init(accum_bar, 1);
     mbar_init(x_bar, 1);
-    mbar_init(w_bar, kThreads);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w);
@@ -160,44 +158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ---------------- before the grid-dependency wait: weights only
-  const int npre = min(n, stages);
-  if (p.lsu_w) {
-    // all threads, 16 bytes each, straight into the 128-byte-swizzled box layout
-    const uint8_t* const wsrc =
-        p.w + static_cast<size_t>(tile) * 128 * p.K + static_cast<size_t>(c_begin) * 128;
-    for (int u = threadIdx.x; u < npre * 1024; u += kThreads) {
-      const int i = u >> 10, r = (u >> 3) & 127, q = u & 7;
-      cp_async_16(base + L.w_off(i) + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4),
-                  wsrc + static_cast<size_t>(r) * p.K + i * 128 + q * 16);
-    }
-    const uint8_t* const ssrc =
-        p.w_scales + (static_cast<size_t>(tile) * p.nchunks + c_begin) * kSfTileBytes;
-    for (int u = threadIdx.x; u < n * 32; u += kThreads)
-      cp_async_16(base + L.sfa_off(0) + u * 16, ssrc + u * 16);
-    cp_async_commit();
-  } else {
-    if (w_lane && lane < n) issue_w(lane, lane);
-    if (warp == 2 && lane == 0) {
-      mbar_expect_tx(sfa_bar, static_cast<uint32_t>(n) * kSfTileBytes);
-      bulk_load(base + L.sfa_off(0),
-                p.w_scales + (static_cast<size_t>(tile) * p.nchunks + c_begin) * kSfTileBytes,
-                static_cast<uint32_t>(n) * kSfTileBytes, sfa_bar, pol_w);
-    }
+  if (w_lane && lane < n) issue_w(lane, lane);
+  if (warp == 0) issued_n = min(n, stages);
+  if (warp == 2 && lane == 0) {
+    mbar_expect_tx(sfa_bar, static_cast<uint32_t>(n) * kSfTileBytes);
+    bulk_load(base + L.sfa_off(0),
+              p.w_scales + (static_cast<size_t>(tile) * p.nchunks + c_begin) * kSfTileBytes,
+              static_cast<uint32_t>(n) * kSfTileBytes, sfa_bar, pol_w);
   }
-  if (warp == 0) issued_n = npre;
   pdl_launch_dependents();
   pdl_wait();
-  if (p.lsu_w) {
-    // each thread's copies have landed; make them visible to the tensor cores
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    mbar_arrive(w_bar);
-    if (w_lane && lane < n) {
-      // stage `lane` now holds its first weight box: the weight half of full(s)
-      if (!mbar_wait(w_bar, 0)) fail();
-      mbar_arrive(full(lane));
-    }
-  }
 
   // ---------------- activations (written by the previous kernel on the stream)
   int x_batches = 0;  // bf16 row batches requested (fused), warp 3
@@ -344,8 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id2 = idesc_mxf8(p.mtile, 2), id3 = idesc_mxf8(p.mtile, 3);
     // every wait below is taken by all lanes and decided by a warp vote, so the
     // warp stays converged for elect.sync and leaves the loop together
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(p.lsu_w ? w_bar : sfa_bar, 0) &&
-                                     (kFusedA || mbar_wait(sfb_bar, 0)))) {
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfa_bar, 0) && (kFusedA || mbar_wait(sfb_bar, 0)))) {
       if (lane == 0) fail();
     } else {
       uint32_t w_lo = static_cast<uint32_t>(wd), a_lo = static_cast<uint32_t>(ad);
@@ -467,10 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_flag != 0) {
     // wait (bounded) for the copies still in flight, so none lands after exit:
     // per stage, the last chunk loaded into it (an earlier one in the same stage
-    // had landed before the stage was refilled); load/store-path copies were
-    // waited for after the grid-dependency wait
+    // had landed before the stage was refilled)
     if (last >= 0 && last + stages >= issued_n) mbar_wait(full(last % stages), (last / stages) & 1);
-    if (warp == 2 && lane == 0 && !p.lsu_w) mbar_wait(sfa_bar, 0);
+    if (warp == 2 && lane == 0) mbar_wait(sfa_bar, 0);
     if (warp == 2 && lane == 1 && !kFusedA) mbar_wait(sfb_bar, 0);
     if (warp == 3 && lane == 0 && x_batches > 0) mbar_wait(x_bar, (x_batches - 1) & 1);
   }
@@ -554,14 +522,6 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a) {
   while (static_cast<size_t>(stages) * L1.stage_bytes + scales < static_cast<size_t>(pl.mtile) * 512)
     ++stages;
   pl.stages = stages;
-  // Optional (MX_LSU_W=1): load the ring's weights through the load/store path
-  // before the dependency wait (TMA copies issued there are held until the
-  // previous grid completes). Measured on GB300: back-to-back decode GEMMs gain
-  // (M = 1: 4.31 -> 4.11 us), but behind a short quantize kernel or in the
-  // projection chain the prefetch traffic delays the kernel in front, and the
-  // step is slower (22.2 -> 23.4 us); off by default.
-  pl.lsu_w = 0;
-  if (const char* e = getenv("MX_LSU_W")) pl.lsu_w = atoi(e) != 0 && per_cta <= stages;
   pl.tmem_cols = pow2_at_least(tmem_sfa_col(pl.mtile) + 4 * stages * (1 + nsfb));
   const Layout L(pl.mtile, stages, per_cta, fused_a, xrows);
   // CTAs that can share an SM must fit their TMEM together: ask for enough

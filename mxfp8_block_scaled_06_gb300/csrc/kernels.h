@@ -31,7 +31,6 @@ struct GemmPlan {
   int splits;
   int stages;
   int tmem_cols;
-  int lsu_w;  // weights of the ring loaded through the load/store path (see GemmArgs)
   size_t smem;
 };
 
@@ -50,11 +49,6 @@ struct GemmArgs {
   // column blocks per row tile (= K / 128 when not grouped).
   int group_tiles;
   int a_sf_chunks;
-  // Weights of the first ring stages (and all weight scale tiles) loaded by all
-  // threads through the load/store path before the grid-dependency wait (they
-  // then land while the previous kernel runs); w = the [N, K] weights. 0 = TMA.
-  int lsu_w;
-  const uint8_t* w;
   void* out;          // bf16 [M, N] or null
   uint8_t* q;         // fused requantization of columns [0, q_cols): E4M3 [M, q_cols]
   uint8_t* q_scales;  // swizzled scales of q

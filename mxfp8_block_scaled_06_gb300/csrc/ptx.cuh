@@ -91,19 +91,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-// ------------------------------------------- load/store-path async copies
-// Unlike TMA copies, these are not held back when a dependent grid issues them
-// before its grid-dependency wait.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
 // ---------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -169,18 +169,52 @@ class Clocks:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sm)}
 
 
+class Replicas:
+    """N independent replicas, one process per GPU (launched by torchrun): the
+    path has no exchange step, so the ranks share only host-side coordination
+    over gloo - a barrier before the timed region and the maximum of the timed
+    region over ranks. Rank 0 alone reports."""
+
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world > 1:
+            import torch.distributed as dist
+            if not dist.is_initialized():
+                dist.init_process_group("gloo", init_method="env://")
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def job_value(self, bytes_per_rank_step: float, ms_step: float) -> float:
+        """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+        return self.world * bytes_per_rank_step / (ms_step * 1e-3) / 1e9
+
+    @property
+    def reports(self) -> bool:
+        return self.rank == 0
+
+
 def run_ours(args):
     import torch
 
     import mxfp8_block_scaled_06_gb300 as mx
     from mxfp8_block_scaled_06_gb300 import build as mxbuild
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo", init_method="env://")
+    rep = Replicas()
+    world, rank, local = rep.world, rep.rank, rep.local
     mxbuild.build()
     torch.cuda.set_device(local)
     h = mx.mx_create(local)
@@ -221,8 +255,7 @@ def run_ours(args):
         while time.time() < t_end:
             g_step.replay()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    rep.barrier()
     torch.cuda.synchronize()
     st, sp = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -233,12 +266,9 @@ def run_ours(args):
     sp.synchronize()
     ms_total = st.elapsed_time(sp)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = rep.max_over_ranks(ms_total)
     ms_step = ms_total / k_eff
-    value = world * step_bytes() / (ms_step * 1e-3) / 1e9
+    value = rep.job_value(step_bytes(), ms_step)
 
     # ------------------------------------------------- per-kernel GEMM timing
     gemm_us, gemm_gbs = {}, {}
@@ -385,10 +415,10 @@ def run_ours(args):
 
     # --------------------------------------------------------- CPU baseline
     cpu = None
-    if rank == 0 and not args.no_cpu:
+    if rep.reports and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.cpu_seconds)
 
-    if rank != 0:
+    if not rep.reports:
         return None
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4),

@@ -1,0 +1,109 @@
+"""Guard canaries around every output of every entry point.
+
+Each output is a view into a larger device buffer whose leading and trailing
+bytes hold a known pattern; after the call the guards must be intact, so a
+kernel writing past either end of an output (wrong index arithmetic, padding
+beyond the documented size) fails here, on shapes with ragged rows and tiles.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import bf16_to_device, handle, quantize_on_gpu
+
+pytestmark = pytest.mark.gpu
+
+PAD = 4096          # guard bytes on each side (keeps 16-byte alignment)
+PATTERN = 0xA5
+
+
+class Guarded:
+    def __init__(self):
+        self.bufs = []
+
+    def u8(self, nbytes):
+        buf = torch.full((nbytes + 2 * PAD,), PATTERN, dtype=torch.uint8, device="cuda")
+        self.bufs.append((buf, nbytes))
+        return buf[PAD:PAD + nbytes]
+
+    def bf16(self, rows, cols):
+        return self.u8(rows * cols * 2).view(torch.bfloat16).view(rows, cols)
+
+    def check(self):
+        torch.cuda.synchronize()
+        for buf, n in self.bufs:
+            host = buf.cpu().numpy()
+            assert (host[:PAD] == PATTERN).all(), "write before the start of an output"
+            assert (host[PAD + n:] == PATTERN).all(), "write past the end of an output"
+
+
+@pytest.mark.parametrize("m,k", [(1, 64), (5, 160), (130, 96), (3, 5120)])
+def test_quantize_rows_guards(m, k):
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    g = Guarded()
+    x = bf16_to_device(synth.block_scaled_bf16(1, synth.TAG_A, m, k, -6, 6))
+    q = g.u8(m * k).view(m, k)
+    s = g.u8(mx.mx_scale_bytes(m, k))
+    mx.mx_quantize_rows(handle(), x, q=q, scales=s)
+    q2 = g.u8(m * k).view(m, k)
+    s2 = g.u8(m * (k // 32))
+    mx.mx_quantize_rows(handle(), x, q=q2, scales=s2, swizzled=False)
+    g.check()
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 2048, 5120), (17, 384, 640), (130, 256, 512), (64, 8192, 1536)])
+def test_gemm_and_bf16_gemm_guards(m, n, k):
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    g = Guarded()
+    abits = synth.block_scaled_bf16(2, synth.TAG_A, m, k, -6, 6)
+    aq, asc = quantize_on_gpu(abits)
+    wq, wsc = quantize_on_gpu(synth.block_scaled_bf16(2, synth.TAG_W, n, k, -6, 6))
+    out = g.bf16(m, n)
+    mx.mx_gemm(handle(), aq, asc, wq, wsc, out=out, pdl=True)
+    out2 = g.bf16(m, n)
+    mx.mx_gemm_bf16(handle(), bf16_to_device(abits), wq, wsc, out=out2)
+    g.check()
+    assert mx.mx_device_status(handle()) == mx.MX_OK
+
+
+@pytest.mark.parametrize("m", [1, 17])
+def test_chain_guards(m):
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    g = Guarded()
+    shapes = [(2048, 5120), (8192, 1536), (5120, 8192)]
+    ws = [quantize_on_gpu(synth.block_scaled_bf16(3 + i, synth.TAG_W, n, k, -6, 6))
+          for i, (n, k) in enumerate(shapes)]
+    a1 = quantize_on_gpu(synth.block_scaled_bf16(3, synth.TAG_A, m, 5120, -4, 4))
+    bufs = dict(out=g.bf16(m, 5120),
+                a2=g.u8(m * 1536).view(m, 1536), a2_scales=g.u8(mx.mx_scale_bytes(m, 1536)),
+                a3=g.u8(m * 8192).view(m, 8192), a3_scales=g.u8(mx.mx_scale_bytes(m, 8192)))
+    mx.mx_gemm_chain(handle(), a1[0], a1[1], ws, **bufs)
+    g.check()
+    assert mx.mx_device_status(handle()) == mx.MX_OK
+
+
+@pytest.mark.parametrize("t", [1, 9, 33])
+def test_wo_a_guards(t):
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    G, H, R, D = 4, 8, 1024, 512
+    g = Guarded()
+    ww = quantize_on_gpu(synth.block_scaled_bf16(4, synth.TAG_WOA, G * R, H * D, -6, 6))
+    cs = torch.from_numpy(synth.rope_cos_sin_cache(65536)).cuda()
+    x = bf16_to_device(synth.normal_bf16(4, synth.TAG_X, (t, G * H, D)))
+    pos = torch.from_numpy(synth.positions(4, synth.TAG_POS, t)).cuda()
+    q = g.u8(t * G * R).view(t, G * R)
+    qs = g.u8(mx.mx_scale_bytes(t, G * R))
+    mx.wo_a_grouped(handle(), x, pos, cs, *ww, G, H, R, q=q, q_scales=qs)
+    q2 = g.u8(t * G * R).view(t, G * R)
+    qs2 = g.u8(mx.mx_scale_bytes(t, G * R))
+    xq = g.u8(t * G * H * D).view(t, G * H * D)
+    xqs = g.u8(mx.mx_scale_bytes(t, G * H * D))
+    mx.wo_a_grouped_unfused(handle(), x, pos, cs, *ww, G, H, R, q=q2, q_scales=qs2, xq=xq,
+                            xq_scales=xqs)
+    g.check()
+    assert mx.mx_device_status(handle()) == mx.MX_OK

@@ -32,6 +32,9 @@ Readings where the pages are silent (each also listed in the design notes):
   - the projection chain rounds each product to bf16 (RNE) before requantizing;
   - WO-A rotates the rope pairs in float32 without fused multiply-add, keeps the
     rotated values in float32 (no bf16 round) and quantizes per 32 elements.
+  - the split between G1 and G2 (``_split_qkv_and_norm``, shown only as a call):
+    qr = G1's first 1536 bf16 columns, RMS-normalized over them with a given
+    weight and epsilon, rounded to bf16, MX-quantized; kv = the other columns.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (exhaustive codec tables, torch's independent float8 cast, brute force, exact
@@ -237,6 +240,40 @@ def chain(a1_codes, a1_sbytes, weights, g1_cols: int = 1536) -> dict:
     out3 = mx_gemm(a3, a3s, w3, s3)
     return dict(out1=out1, b1=b1, a2=a2, a2s=a2s, out2=out2, b2=b2, a3=a3, a3s=a3s,
                 out3=out3, b3=round_bf16(out3))
+
+
+def rms_norm(x, weight, eps: float) -> np.ndarray:
+    """Each row over its last axis: x / sqrt(mean(x^2) + eps) * weight, float64."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(weight, dtype=np.float64)
+
+
+def split_qkv_and_norm(out1_bf16, norm_weight, eps: float, q_cols: int = 1536) -> dict:
+    """The split between the first two projections (`_split_qkv_and_norm` in
+    `AttentionStep.run`; reading: the pages show only its call). qr = the first
+    q_cols columns of G1's bf16 output, RMS-normalized over those columns with
+    the given weight and epsilon, rounded to bf16 and MX-quantized for G2; kv =
+    the remaining columns, unchanged."""
+    out1_bf16 = np.asarray(out1_bf16, dtype=np.float64)
+    y = round_bf16(rms_norm(out1_bf16[:, :q_cols], norm_weight, eps))
+    q, qs = mx_quantize(y)
+    return dict(y=y, q=q, qs=qs, kv=out1_bf16[:, q_cols:])
+
+
+def chain_norm(a1_codes, a1_sbytes, weights, norm_weight, eps: float, g1_cols: int = 1536) -> dict:
+    """`chain` with the split-and-norm between G1 and G2 instead of the plain
+    requantization of G1's first g1_cols columns."""
+    (w1, s1), (w2, s2), (w3, s3) = weights
+    out1 = mx_gemm(a1_codes, a1_sbytes, w1, s1)
+    b1 = round_bf16(out1)
+    sp = split_qkv_and_norm(b1, norm_weight, eps, g1_cols)
+    out2 = mx_gemm(sp["q"], sp["qs"], w2, s2)
+    b2 = round_bf16(out2)
+    a3, a3s = mx_quantize(b2)
+    out3 = mx_gemm(a3, a3s, w3, s3)
+    return dict(out1=out1, b1=b1, y=sp["y"], a2=sp["q"], a2s=sp["qs"], kv=sp["kv"], out2=out2,
+                b2=b2, a3=a3, a3s=a3s, out3=out3, b3=round_bf16(out3))
 
 
 # ----------------------------------------------------------------------------

@@ -359,3 +359,40 @@ def test_wo_a_tiny_brute_force():
             assert abs(Fraction(float(got["z"][0, gg * r + j])) - ex[0][j]) <= abs(ex[0][j]) * Fraction(2) ** -40 + Fraction(2) ** -200
     qc, qs = oracle.mx_quantize(got["zb"])
     np.testing.assert_array_equal(got["q"], qc)
+
+
+# ------------------------------------------------------------ RMS norm split
+def test_rms_norm_closed_forms():
+    # [3, 4]: mean square 12.5, so y = (3, 4) / (5 / sqrt 2) = (3 sqrt2 / 5, 4 sqrt2 / 5)
+    y = oracle.rms_norm(np.array([[3.0, 4.0]]), np.ones(2), 0.0)
+    np.testing.assert_allclose(y[0], [3 * np.sqrt(2) / 5, 4 * np.sqrt(2) / 5], rtol=0, atol=1e-15)
+    # a constant row normalizes to the weight itself (eps = 0), with the row's sign
+    w = np.array([0.5, -2.0, 3.0, 1.0])
+    np.testing.assert_array_equal(oracle.rms_norm(np.full((1, 4), -7.25), w, 0.0)[0], -w)
+    # a zero row stays zero with eps > 0
+    assert (oracle.rms_norm(np.zeros((1, 8)), np.ones(8), 1e-6) == 0).all()
+
+
+def test_rms_norm_invariants():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((4, 96))
+    y = oracle.rms_norm(x, np.ones(96), 0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=-1), 1.0, rtol=1e-13)  # unit RMS
+    for k in (-20, -3, 5, 40):  # scale invariance: powers of two scale exactly
+        np.testing.assert_array_equal(oracle.rms_norm(np.ldexp(x, k), np.ones(96), 0.0), y)
+    # eps lowers the result toward zero, by sqrt(ms / (ms + eps))
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    np.testing.assert_allclose(oracle.rms_norm(x, np.ones(96), 0.25), y * np.sqrt(ms / (ms + 0.25)),
+                               rtol=1e-13)
+
+
+def test_split_qkv_and_norm_parts():
+    rng = np.random.default_rng(6)
+    out1 = oracle.round_bf16(rng.standard_normal((3, 2048)) * 4)
+    w = oracle.round_bf16(rng.uniform(0.5, 1.5, 1536))
+    sp = oracle.split_qkv_and_norm(out1, w, 1e-6)
+    np.testing.assert_array_equal(sp["kv"], out1[:, 1536:])
+    assert sp["y"].shape == (3, 1536) and (oracle.round_bf16(sp["y"]) == sp["y"]).all()
+    q2, s2 = oracle.mx_quantize(sp["y"])
+    np.testing.assert_array_equal(sp["q"], q2)
+    np.testing.assert_array_equal(sp["qs"], s2)

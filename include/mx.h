@@ -90,6 +90,22 @@ size_t mx_scale_bytes(int rows, int k);
 int mx_quantize_rows(mx_handle* h, int M, int K, const void* x, long ldx,
                      void* q, void* scales, int swizzled, void* stream);
 
+/* RMS normalization then MX quantization of each row: y = bf16(x / sqrt(mean
+ * over the row of x^2 + eps) * norm_weight), computed in float32, then y
+ * quantized as mx_quantize_rows does. This is the split between the first two
+ * projections of a decode step (`qr, qr_scale, kv = attn._split_qkv_and_norm(
+ * qr_kv)` in `AttentionStep.run`, step page; the pages show only the call: the
+ * reading is an RMS norm of qr with a given weight and epsilon).
+ *   x           [M, K] bf16, row stride ldx elements (ldx >= K, ldx % 8 == 0),
+ *               16-byte aligned.
+ *   norm_weight [K] bf16, 16-byte aligned; eps >= 0.
+ *   y           optional [M, K] bf16 out (row stride K), or null.
+ *   q, scales   as in mx_quantize_rows.
+ * Constraints: 1 <= M <= 65536, K % 32 == 0. */
+int mx_rmsnorm_quantize_rows(mx_handle* h, int M, int K, const void* x, long ldx,
+                             const void* norm_weight, float eps, void* y, void* q,
+                             void* scales, int swizzled, void* stream);
+
 /* out = dequant(A) x dequant(W)^T (`launch_low_latency`: out = a times the
  * column-major [K, N] weight; bf16 out, float32 accumulation, no scale/bias).
  *   a        [M, K] E4M3, row stride K, 16-byte aligned.
@@ -139,6 +155,21 @@ int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales,
                   const mx_weight w[3], int g1_cols, void* a2, void* a2_scales,
                   void* a3, void* a3_scales, void* out, void* debug_out1,
                   void* debug_out2, void* stream);
+
+/* mx_gemm_chain with the split between G1 and G2 of `AttentionStep.run`:
+ * G1 writes its whole bf16 output to out1 ([M, N1]: qr = columns [0, g1_cols),
+ * kv = the rest, which the caller reads from out1), qr is RMS-normalized with
+ * norm_weight / eps and MX-quantized into a2 / a2_scales
+ * (mx_rmsnorm_quantize_rows), then G2 (+ requantization into a3) and G3 as in
+ * mx_gemm_chain. Four launches on one stream, with PDL.
+ *   norm_weight [g1_cols] bf16, 16-byte aligned; eps >= 0.
+ *   out1        [M, N1] bf16, required.
+ *   debug_y     optional [M, g1_cols] bf16: the normalized qr before quantization.
+ * Other arguments and constraints as in mx_gemm_chain. */
+int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scales,
+                       const mx_weight w[3], int g1_cols, const void* norm_weight, float eps,
+                       void* out1, void* a2, void* a2_scales, void* a3, void* a3_scales,
+                       void* out, void* debug_y, void* debug_out2, void* stream);
 
 /* Grouped WO-A with RoPE, writing MXFP8 for wo_b (`dsv41_o_proj` and
  * `_can_fuse_wo_a` on the page "vllm.models.deepseek_v41.nvidia.ops.o_proj").

@@ -19,8 +19,9 @@ LIB_PATH = os.path.join(HERE, "libmx.so")
 MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_DEVICE, MX_ERR_CUDA, MX_ERR_TIMEOUT = range(6)
 MX_FLAG_PDL = 1
 
-EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows", "mx_gemm", "mx_gemm_bf16",
-           "mx_gemm_chain", "wo_a_grouped", "wo_a_grouped_unfused", "mx_device_status",
+EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows",
+           "mx_rmsnorm_quantize_rows", "mx_gemm", "mx_gemm_bf16", "mx_gemm_chain",
+           "mx_gemm_chain_norm", "wo_a_grouped", "wo_a_grouped_unfused", "mx_device_status",
            "mx_status_string"]
 
 _vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
@@ -53,6 +54,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx_scale_bytes.restype = ctypes.c_size_t
     lib.mx_quantize_rows.argtypes = [_vp, _i, _i, _vp, _l, _vp, _vp, _i, _vp]
     lib.mx_gemm.argtypes = [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _u, _vp]
+    lib.mx_rmsnorm_quantize_rows.argtypes = [_vp, _i, _i, _vp, _l, _vp, ctypes.c_float, _vp, _vp,
+                                             _vp, _i, _vp]
+    lib.mx_gemm_chain_norm.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp,
+                                       ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.mx_gemm_bf16.argtypes = [_vp, _i, _i, _i, _vp, _l, _vp, _vp, _vp, _u, _vp]
     lib.mx_gemm_chain.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp]
@@ -184,6 +189,52 @@ def mx_gemm_chain(h: Handle, a1, a1_scales, weights, g1_cols: int = 1536, out=No
                                         _ptr(a2_scales), _ptr(a3), _ptr(a3_scales), _ptr(out),
                                         _ptr(d1), _ptr(d2), _stream(stream)), "mx_gemm_chain")
     return dict(out=out, a2=a2, a2_scales=a2_scales, a3=a3, a3_scales=a3_scales, out1=d1, out2=d2)
+
+
+def mx_rmsnorm_quantize_rows(h: Handle, x, norm_weight, eps: float, q=None, scales=None,
+                             swizzled: bool = True, y: bool = False, stream=None):
+    """bf16 [M, K] (row stride x.stride(0)) -> RMS-normalized with norm_weight [K] bf16 and
+    eps, rounded to bf16 (returned as y when asked) and MX-quantized: (q, scales, y)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    m, k = x.shape
+    if q is None:
+        q = _empty_u8((m, k), x.device)
+    if scales is None:
+        scales = _empty_u8((mx_scale_bytes(m, k),) if swizzled else (m, k // 32), x.device)
+    yt = torch.empty((m, k), dtype=torch.bfloat16, device=x.device) if y else None
+    _check(load_library().mx_rmsnorm_quantize_rows(h.ptr, m, k, _ptr(x), x.stride(0),
+                                                   _ptr(norm_weight), float(eps), _ptr(yt), _ptr(q),
+                                                   _ptr(scales), int(swizzled), _stream(stream)),
+           "mx_rmsnorm_quantize_rows")
+    return q, scales, yt
+
+
+def mx_gemm_chain_norm(h: Handle, a1, a1_scales, weights, norm_weight, eps: float,
+                       g1_cols: int = 1536, out=None, out1=None, a2=None, a2_scales=None, a3=None,
+                       a3_scales=None, debug: bool = False, stream=None) -> dict:
+    """mx_gemm_chain with the RMS-norm split between G1 and G2: G1's bf16 output goes
+    to out1 (qr | kv), qr is normalized and quantized for G2."""
+    import torch
+    m = a1.shape[0]
+    dev = a1.device
+    ws = (MxWeight * 3)(*[MxWeight(_ptr(w), _ptr(s), w.shape[0], w.shape[1]) for w, s in weights])
+    n1, n2, n3 = (w.shape[0] for w, _ in weights)
+    out1 = torch.empty((m, n1), dtype=torch.bfloat16, device=dev) if out1 is None else out1
+    a2 = _empty_u8((m, g1_cols), dev) if a2 is None else a2
+    a2_scales = _empty_u8((mx_scale_bytes(m, g1_cols),), dev) if a2_scales is None else a2_scales
+    a3 = _empty_u8((m, n2), dev) if a3 is None else a3
+    a3_scales = _empty_u8((mx_scale_bytes(m, n2),), dev) if a3_scales is None else a3_scales
+    out = torch.empty((m, n3), dtype=torch.bfloat16, device=dev) if out is None else out
+    dy = torch.empty((m, g1_cols), dtype=torch.bfloat16, device=dev) if debug else None
+    d2 = torch.empty((m, n2), dtype=torch.bfloat16, device=dev) if debug else None
+    _check(load_library().mx_gemm_chain_norm(h.ptr, m, _ptr(a1), _ptr(a1_scales), ws, g1_cols,
+                                             _ptr(norm_weight), float(eps), _ptr(out1), _ptr(a2),
+                                             _ptr(a2_scales), _ptr(a3), _ptr(a3_scales), _ptr(out),
+                                             _ptr(dy), _ptr(d2), _stream(stream)),
+           "mx_gemm_chain_norm")
+    return dict(out=out, out1=out1, a2=a2, a2_scales=a2_scales, a3=a3, a3_scales=a3_scales, y=dy,
+                out2=d2)
 
 
 def wo_a_grouped(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,

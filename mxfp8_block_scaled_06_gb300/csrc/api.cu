@@ -177,6 +177,21 @@ int mx_quantize_rows(mx_handle* h, int M, int K, const void* x, long ldx, void* 
                                               static_cast<cudaStream_t>(stream)));
 }
 
+int mx_rmsnorm_quantize_rows(mx_handle* h, int M, int K, const void* x, long ldx,
+                             const void* norm_weight, float eps, void* y, void* q, void* scales,
+                             int swizzled, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (M < 1 || M > 65536 || K < 32 || K % 32 != 0 || ldx < K || ldx % 8 != 0)
+    return MX_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || x == nullptr || norm_weight == nullptr || q == nullptr || scales == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(norm_weight, 16) || !aligned(q, 16) || (y && !aligned(y, 16)))
+    return MX_ERR_INVALID_ARG;
+  return cuda_status(mx::launch_rmsnorm_quantize_rows(x, ldx, M, K, norm_weight, eps, y, q, scales,
+                                                      swizzled, static_cast<cudaStream_t>(stream)));
+}
+
 int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales, const void* w,
             const void* w_scales, void* out, unsigned flags, void* stream) {
   int rc = check_device(h);
@@ -226,6 +241,41 @@ int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, co
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = gemm_launch(h, M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, debug_out1,
                    static_cast<uint8_t*>(a2), static_cast<uint8_t*>(a2_scales), g1_cols, true, s);
+  if (rc != MX_OK) return rc;
+  rc = gemm_launch(h, M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
+                   static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n, true, s);
+  if (rc != MX_OK) return rc;
+  return gemm_launch(h, M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
+                     nullptr, 0, true, s);
+}
+
+int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scales,
+                       const mx_weight w[3], int g1_cols, const void* norm_weight, float eps,
+                       void* out1, void* a2, void* a2_scales, void* a3, void* a3_scales, void* out,
+                       void* debug_y, void* debug_out2, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (w == nullptr || norm_weight == nullptr || out1 == nullptr || !(eps >= 0.f))
+    return MX_ERR_INVALID_ARG;
+  rc = validate_gemm(h, M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales);
+  if (rc != MX_OK) return rc;
+  rc = validate_gemm(h, M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales);
+  if (rc != MX_OK) return rc;
+  rc = validate_gemm(h, M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales);
+  if (rc != MX_OK) return rc;
+  if (g1_cols < 128 || g1_cols % 128 != 0 || g1_cols > w[0].n || w[1].k != g1_cols ||
+      w[2].k != w[1].n)
+    return MX_ERR_INVALID_ARG;
+  if (out == nullptr || !aligned(out, 16) || !aligned(out1, 16) || !aligned(norm_weight, 16) ||
+      (debug_y && !aligned(debug_y, 16)) || (debug_out2 && !aligned(debug_out2, 16)))
+    return MX_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // G1 -> bf16 out1 (qr | kv); RMS norm of qr + MX quantize -> a2; G2 (+ requant) -> a3; G3
+  rc = gemm_launch(h, M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, out1, nullptr,
+                   nullptr, 0, true, s);
+  if (rc != MX_OK) return rc;
+  rc = cuda_status(mx::launch_rmsnorm_quantize_rows(out1, w[0].n, M, g1_cols, norm_weight, eps,
+                                                    debug_y, a2, a2_scales, 1, s));
   if (rc != MX_OK) return rc;
   rc = gemm_launch(h, M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
                    static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n, true, s);

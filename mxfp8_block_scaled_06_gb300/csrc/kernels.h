@@ -23,6 +23,12 @@ cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q,
                                  int swizzled, cudaStream_t stream,
                                  const RopeArgs& rope = RopeArgs{nullptr, nullptr, 0, 0, 0, nullptr});
 
+// y = bf16(x / sqrt(mean(x^2) + eps) * gamma) per row (float32 arithmetic), then
+// MX-quantized into q / scales; y may be null.
+cudaError_t launch_rmsnorm_quantize_rows(const void* x, long ldx, int M, int K, const void* gamma,
+                                         float eps, void* y, void* q, void* scales, int swizzled,
+                                         cudaStream_t stream);
+
 // ------------------------------------------------------------ block-scaled GEMM
 // Plan of one GEMM launch: activation tile (MMA N), K-splits per weight tile
 // (a thread-block cluster along K), pipeline depth, TMEM columns, shared bytes.

@@ -106,7 +106,128 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 }
 
+// RMS normalization + MX quantization of rows (the split between the first two
+// decode projections): one warp per row; pass 1 sums the squares of the row in
+// float32 (each lane over its units in order, then xor-shuffles: a fixed order),
+// pass 2 scales each element by 1/sqrt(mean + eps) (correctly rounded sqrt and
+// division) and the row's weight, rounds to bf16 (optionally stored) and
+// quantizes per 32-block as quantize_rows_kernel does.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    rmsnorm_quantize_rows_kernel(const uint16_t* __restrict__ x, long ldx, int M, int K,
+                                 const uint16_t* __restrict__ gamma, float eps,
+                                 uint16_t* __restrict__ y, uint8_t* __restrict__ q,
+                                 uint8_t* __restrict__ scales, int swizzled, int rows_total) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int row = static_cast<int>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows_total) return;  // warp-uniform
+  const int nblk = K >> 5;
+  const int cpad4 = (nblk + 3) & ~3;
+  const int groups = (cpad4 + 7) / 8;  // 8 blocks (256 elements) per pass of the warp
+  const bool real = row < M;
+  const uint16_t* const xr = x + static_cast<size_t>(row) * ldx;
+  float ss = 0.f;
+  if (real) {
+    for (int g = 0; g < groups; ++g) {
+      const int blk = g * 8 + (lane >> 2);
+      if (blk >= nblk) continue;
+      const uint4 raw = *reinterpret_cast<const uint4*>(xr + blk * 32 + (lane & 3) * 8);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
+        ss = __fadd_rn(ss, __fmul_rn(a, a));
+        ss = __fadd_rn(ss, __fmul_rn(b, b));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
+  const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps)));
+  for (int g = 0; g < groups; ++g) {
+    const int blk = g * 8 + (lane >> 2);
+    const int sub = lane & 3;
+    const bool valid = real && blk < nblk;
+    float v[8];
+    float amax = 0.f;
+    uint32_t nonfinite = 0;
+    if (valid) {
+      const int k0 = blk * 32 + sub * 8;
+      const uint4 raw = *reinterpret_cast<const uint4*>(xr + k0);
+      const uint4 graw = *reinterpret_cast<const uint4*>(gamma + k0);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
+      uint32_t packed[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = __fmul_rn(__fmul_rn(__uint_as_float(w[i] << 16), inv), __uint_as_float(gw[i] << 16));
+        const float b = __fmul_rn(__fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv),
+                                  __uint_as_float(gw[i] & 0xFFFF0000u));
+        const uint32_t ha = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+        packed[i] = ha | (hb << 16);
+        v[2 * i] = __uint_as_float(ha << 16);
+        v[2 * i + 1] = __uint_as_float(hb << 16);
+      }
+      if (y != nullptr)
+        *reinterpret_cast<uint4*>(y + static_cast<size_t>(row) * K + k0) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        amax = fmaxf(amax, fabsf(v[i]));
+        nonfinite |= !isfinite(v[i]);
+      }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 1);
+    nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 2);
+    uint32_t sbyte = 0;
+    if (valid) {
+      uint32_t lo, hi;
+      if (nonfinite) {
+        sbyte = 0xFFu;
+        lo = hi = 0x7F7F7F7Fu;
+      } else {
+        sbyte = mx_scale_byte(amax);
+        const float f = mx_inv_scale(sbyte);
+        lo = cvt_e4m3x2(v[0] * f, v[1] * f) | (cvt_e4m3x2(v[2] * f, v[3] * f) << 16);
+        hi = cvt_e4m3x2(v[4] * f, v[5] * f) | (cvt_e4m3x2(v[6] * f, v[7] * f) << 16);
+      }
+      *reinterpret_cast<uint2*>(q + static_cast<size_t>(row) * K + blk * 32 + sub * 8) =
+          make_uint2(lo, hi);
+    }
+    if (sub == 0) {
+      if (swizzled) {
+        if (blk < cpad4) scales[swz_offset(row, blk, cpad4)] = static_cast<uint8_t>(sbyte);
+      } else if (valid) {
+        scales[static_cast<size_t>(row) * nblk + blk] = static_cast<uint8_t>(sbyte);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rmsnorm_quantize_rows(const void* x, long ldx, int M, int K, const void* gamma,
+                                         float eps, void* y, void* q, void* scales, int swizzled,
+                                         cudaStream_t stream) {
+  const int rows_total = swizzled ? ((M + 127) / 128) * 128 : M;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows_total + kWarpsPerBlock - 1) / kWarpsPerBlock), 1, 1);
+  cfg.blockDim = dim3(kWarpsPerBlock * 32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rmsnorm_quantize_rows_kernel, static_cast<const uint16_t*>(x), ldx,
+                            M, K, static_cast<const uint16_t*>(gamma), eps, static_cast<uint16_t*>(y),
+                            static_cast<uint8_t*>(q), static_cast<uint8_t*>(scales), swizzled,
+                            rows_total);
+}
 
 cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q, void* scales,
                                  int swizzled, cudaStream_t stream, const RopeArgs& rope) {

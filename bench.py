@@ -322,6 +322,15 @@ def run_ours(args):
             us = ms * 1e3 / 300
             chain[m] = {"us": round(us, 3), "weight_gbs": round(wbytes / (us * 1e-6) / 1e9, 1),
                         "vs_weight_read_at_peak": round(us / (wbytes / (pk["hbm_gbs"] * 1e9) * 1e6), 3)}
+            # the same chain with the RMS-norm split between G1 and G2 (one more launch)
+            out1 = torch.empty((m, CHAIN_SHAPES[0][0]), dtype=torch.bfloat16, device=rig.dev)
+            nw = torch.ones(CHAIN_G1_COLS, dtype=torch.bfloat16, device=rig.dev)
+
+            def run_norm(i, m=m, q1=q1, bufs=bufs, out1=out1, nw=nw):
+                mx.mx_gemm_chain_norm(h, q1[0], q1[1], cw[i % cset], nw, 1e-6, g1_cols=CHAIN_G1_COLS,
+                                      out1=out1, stream=stream, **bufs)
+            ms, _ = time_graph(torch, run_norm, 5, 60, stream)
+            chain[m]["with_rms_norm_split_us"] = round(ms * 1e3 / 300, 3)
 
     # ------------------------------------------------------- WO-A and wo_b
     woa = {}

@@ -21,6 +21,7 @@ namespace mx {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kPadRows = 8;  // swizzled-scale padding rows zeroed by one warp
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     quantize_rows_kernel(const uint16_t* __restrict__ x, long ldx, int M, int K,
@@ -33,11 +34,20 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   pdl_wait();
   const long gw = static_cast<long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int row = static_cast<int>(gw / groups_per_row);
-  const int grp = static_cast<int>(gw % groups_per_row);
-  if (row >= rows_total) return;  // warp-uniform
   const int nblk = K >> 5;
   const int cpad4 = (nblk + 3) & ~3;
+  const long real_warps = static_cast<long>(M) * groups_per_row;
+  if (gw >= real_warps) {
+    // padding rows [M, rows_total) of the swizzled scales: zero, kPadRows rows per warp
+    const long pw = gw - real_warps;
+    const int r0 = M + static_cast<int>(pw / groups_per_row) * kPadRows;
+    const int blk = static_cast<int>(pw % groups_per_row) * 8 + (lane >> 2);
+    if (r0 >= rows_total || (lane & 3) != 0 || blk >= cpad4) return;
+    for (int r = r0; r < min(r0 + kPadRows, rows_total); ++r) scales[swz_offset(r, blk, cpad4)] = 0;
+    return;
+  }
+  const int row = static_cast<int>(gw / groups_per_row);
+  const int grp = static_cast<int>(gw % groups_per_row);
   const int blk = grp * 8 + (lane >> 2);
   const int sub = lane & 3;
   const bool valid = row < M && blk < nblk;
@@ -235,7 +245,8 @@ cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q,
   const int cols = swizzled ? ((nblk + 3) & ~3) : nblk;
   const int groups_per_row = (cols + 7) / 8;
   const int rows_total = swizzled ? ((M + 127) / 128) * 128 : M;
-  const long warps = static_cast<long>(rows_total) * groups_per_row;
+  const long pad_warps = static_cast<long>((rows_total - M + kPadRows - 1) / kPadRows) * groups_per_row;
+  const long warps = static_cast<long>(M) * groups_per_row + pad_warps;
   const long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);

@@ -66,7 +66,9 @@ typedef struct mx_weight {
 
 /* Create a handle for `device`. Checks compute capability 10.3 (the device
  * gate of `_cute_dsl_runner` / `_wide_supported` on the mxfp8 page), loads the
- * kernels and allocates the 4-byte device status word.
+ * kernels and allocates the 4-byte device status word. The handle also caches
+ * the tensor maps of the buffers it has seen (host memory only), so one handle
+ * is used by one host thread at a time; give each thread its own handle.
  * Returns MX_ERR_DEVICE on another architecture, MX_ERR_CUDA if no device. */
 int mx_create(mx_handle** h, int device);
 int mx_destroy(mx_handle* h);

@@ -9,11 +9,27 @@
 #include "../../include/mx.h"
 #include "kernels.h"
 
+// Tensor maps already encoded by this handle, by (address, rows, k, box rows):
+// an eager caller reuses the same weight and activation buffers call after call,
+// and encoding a map is host work on every launch otherwise. A map holds no
+// device state, so a reused address with the same geometry gets the same map.
+struct TmapEntry {
+  const void* ptr;
+  int rows;
+  long k;
+  int box_rows;
+  CUtensorMap map;
+};
+constexpr int kTmapCache = 32;
+
 struct mx_handle {
   int device;
   int sm_count;
   int* d_status;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
+  TmapEntry tmaps[kTmapCache];
+  int tmap_count;
+  int tmap_next;  // round-robin replacement
 };
 
 namespace {
@@ -31,8 +47,14 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 
 // 2-D uint8 tensor map over a row-major [rows, k] matrix, box {128 bytes, box_rows}
 // with the 128-byte swizzle; out-of-range rows of a box read as zero.
-int make_tmap(const mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, long k,
-              int box_rows) {
+int make_tmap(mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, long k, int box_rows) {
+  for (int i = 0; i < h->tmap_count; ++i) {
+    const TmapEntry& e = h->tmaps[i];
+    if (e.ptr == ptr && e.rows == rows && e.k == k && e.box_rows == box_rows) {
+      *tm = e.map;
+      return MX_OK;
+    }
+  }
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
   cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
@@ -41,7 +63,11 @@ int make_tmap(const mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, lo
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return MX_ERR_CUDA;
+  const int slot = h->tmap_count < kTmapCache ? h->tmap_count++ : h->tmap_next;
+  if (h->tmap_count == kTmapCache) h->tmap_next = (slot + 1) % kTmapCache;
+  h->tmaps[slot] = TmapEntry{ptr, rows, k, box_rows, *tm};
+  return MX_OK;
 }
 
 int validate_gemm(const mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,

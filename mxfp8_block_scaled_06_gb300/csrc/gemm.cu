@@ -5,24 +5,34 @@
 // Swap-AB: the 128 weight rows of a tile are the MMA's M (the only M the
 // block-scaled tcgen05.mma takes with one CTA) and the activation rows,
 // padded to a multiple of 16, are the MMA's N, so 1..256 rows cost one MMA
-// shape. The kernel is bound by the weight stream from HBM; everything below
-// is arranged around keeping that stream saturated:
+// shape. The kernel is bound by the weight stream from HBM and by fixed
+// latencies; everything below is arranged around those:
 //  * grid = (N/128 weight tiles) x (K splits); the splits of one tile form a
 //    thread-block cluster and reduce their partial sums through distributed
-//    shared memory (no global workspace, no second kernel);
-//  * one thread issues TMA loads of 128x128-byte weight boxes (SWIZZLE_128B)
-//    and 512-byte scale tiles for the whole pipeline depth BEFORE the
-//    programmatic-dependent-launch wait, so under PDL the weight read overlaps
-//    the previous kernel on the stream; activations (produced by that kernel)
-//    are loaded only after the wait;
-//  * one thread issues tcgen05.cp (scales -> TMEM) and four
-//    tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each) per 128-wide chunk,
-//    and frees the stage with tcgen05.commit;
+//    shared memory (no global workspace, no second kernel); the split count and
+//    ring depth come from plan_gemm (a measured table for the decode shapes);
+//  * copies issued by one thread are serviced one after another, so each ring
+//    stage has its own issuing lane: warp 0 streams the 128x128-byte weight
+//    boxes (SWIZZLE_128B), the first ring-full before the programmatic
+//    grid-dependency wait; warp 3 the activation boxes after it (they are the
+//    previous kernel's output); warp 2 the scale tiles of the whole K-range,
+//    one bulk copy per operand; refills come from warp-uniform loops whose
+//    issuing lane rotates;
+//  * the MMA warp walks the chunks warp-uniformly and an elected lane issues
+//    tcgen05.cp (scales -> TMEM) and four tcgen05.mma.kind::mxf8f6f4.block_scale
+//    (K = 32 each) per chunk, with the smem descriptors advanced by 32-bit adds
+//    (that one thread's instruction latency bounds the loop), then frees the
+//    stage with tcgen05.commit;
 //  * the four warps read the fp32 accumulator from TMEM (warp w owns lanes
 //    32w..32w+31 = weight rows), stage it in shared memory, and after a cluster
 //    barrier each (row, 32-column block) of the output is summed over the
-//    cluster's partials by one warp; the optional fused requantization (the
-//    chain's next MXFP8 activation) takes the warp's 32 values as one block.
+//    cluster's partials in rank order by one warp; the optional fused
+//    requantization (the chain's next MXFP8 activation) takes the warp's 32
+//    values as one block; a relaxed cluster barrier keeps every CTA alive until
+//    its peers have read its partials.
+// Variants: bf16 activations quantized in the prologue into resident operand
+// tiles (kFusedA), and grouped activations (weight tile t contracts the K-slice
+// of its group of a wider activation).
 // Every mbarrier wait is bounded; on expiry the kernel records MX_ERR_TIMEOUT,
 // skips the remaining work, drains its outstanding copies and frees TMEM.
 #include <cuda_bf16.h>

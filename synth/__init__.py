@@ -104,5 +104,10 @@ def rope_cos_sin_cache(max_pos: int = 65536, rope_dim: int = 64, base: float = 1
 
 
 # Tags keep the tensors of one workload on independent streams.
-TAG_A, TAG_W, TAG_W2, TAG_W3, TAG_X, TAG_POS, TAG_WOA, TAG_WOB = (
-    1 << 8, 2 << 8, 3 << 8, 4 << 8, 5 << 8, 6 << 8, 7 << 8, 8 << 8)
+TAG_A, TAG_W, TAG_W2, TAG_W3, TAG_X, TAG_POS, TAG_WOA, TAG_WOB, TAG_NORM = (
+    1 << 8, 2 << 8, 3 << 8, 4 << 8, 5 << 8, 6 << 8, 7 << 8, 8 << 8, 9 << 8)
+
+
+def norm_weight_bf16(seed: int, k: int) -> np.ndarray:
+    """bf16 bits of a norm weight vector, uniform in [0.5, 1.5)."""
+    return to_bf16_bits(0.5 + uniform01(seed, TAG_NORM, k))

@@ -27,8 +27,7 @@ def _bits(t):
 
 
 def _weight(k, seed):
-    rng = np.random.default_rng(seed)
-    return oracle.bf16_bits(oracle.round_bf16(rng.uniform(0.5, 1.5, k)))
+    return synth.norm_weight_bf16(seed, k)
 
 
 def _run(m, k, seed, eps=1e-6, ldx=None, swizzled=True):

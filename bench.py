@@ -331,7 +331,8 @@ def run_ours(args):
                         "vs_weight_read_at_peak": round(us / (wbytes / (pk["hbm_gbs"] * 1e9) * 1e6), 3)}
             # the same chain with the RMS-norm split between G1 and G2 (one more launch)
             out1 = torch.empty((m, CHAIN_SHAPES[0][0]), dtype=torch.bfloat16, device=rig.dev)
-            nw = torch.ones(CHAIN_G1_COLS, dtype=torch.bfloat16, device=rig.dev)
+            nwb = synth.norm_weight_bf16(4, CHAIN_G1_COLS)
+            nw = torch.from_numpy(nwb.view(np.int16)).view(torch.bfloat16).to(rig.dev)
 
             def run_norm(i, m=m, q1=q1, bufs=bufs, out1=out1, nw=nw):
                 mx.mx_gemm_chain_norm(h, q1[0], q1[1], cw[i % cset], nw, 1e-6, g1_cols=CHAIN_G1_COLS,

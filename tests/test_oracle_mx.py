@@ -2,6 +2,7 @@
 WO-A against brute force, exact rational arithmetic, closed forms and
 invariants (none of them re-calls the function under test)."""
 import math
+from decimal import Decimal, getcontext
 from fractions import Fraction
 
 import numpy as np
@@ -240,6 +241,37 @@ def test_tolerance_rule():
 
 
 # ---------------------------------------------------------------------- chain
+def _nearest_bf16(v: Fraction) -> float:
+    """The bf16 number nearest the rational v, ties to the even significand,
+    found by searching the bf16 neighbours of v's float32 neighbours."""
+    f = float(v)
+    cands = {f, float(np.nextafter(np.float32(f), np.float32(np.inf))),
+             float(np.nextafter(np.float32(f), np.float32(-np.inf)))}
+    bf = set()
+    for c in cands:
+        b = np.array([c], np.float32).view(np.uint32)[0] & np.uint32(0xFFFF0000)
+        for d in (0, 1, -1):
+            bb = np.uint32(int(b) + d * 0x10000)
+            bf.add(float(np.array([bb], np.uint32).view(np.float32)[0]))
+    return min(bf, key=lambda y: (abs(Fraction(y) - v), (np.array([y], np.float32).view(np.uint32)[0] >> 16) & 1))
+
+
+def _exact_stage(ac, asb, wc, wsb) -> np.ndarray:
+    """One projection evaluated exactly with rationals, rounded once to bf16."""
+    ex = oracle.mx_gemm_exact(ac, asb, wc, wsb)
+    return np.array([[_nearest_bf16(v) for v in row] for row in ex])
+
+
+def _brute_requant(b, cols):
+    """(codes [rows][32-blocks], scale bytes) of b's first cols columns by brute force."""
+    blocks = [_brute_block(b[r, 32 * c:32 * c + 32]) for r in range(b.shape[0]) for c in range(cols // 32)]
+    return [c for c, _ in blocks], [s for _, s in blocks]
+
+
+def _blocks(codes):
+    return [[int(x) for x in blk] for blk in np.asarray(codes).reshape(-1, 32)]
+
+
 def test_chain_tiny_brute_force():
     m, k1, n1, g1, n2, n3 = 2, 64, 96, 64, 64, 32
     a = synth.bf16_bits_to_f64(synth.block_scaled_bf16(5, 1, m, k1, -4, 4))
@@ -249,33 +281,17 @@ def test_chain_tiny_brute_force():
     wq = [oracle.mx_quantize(w) for w in ws]
     got = oracle.chain(aq[0], aq[1], wq, g1_cols=g1)
 
-    def stage(ac, asb, wc, wsb):
-        ex = oracle.mx_gemm_exact(ac, asb, wc, wsb)
-        # nearest bf16 of the exact rational, ties to even, by search over neighbours
-        out = np.zeros((len(ex), len(ex[0])))
-        for i, row in enumerate(ex):
-            for j, v in enumerate(row):
-                f = float(v)
-                cands = {f, float(np.nextafter(np.float32(f), np.float32(np.inf))),
-                         float(np.nextafter(np.float32(f), np.float32(-np.inf)))}
-                bf = set()
-                for c in cands:
-                    b = np.array([c], np.float32).view(np.uint32)[0] & np.uint32(0xFFFF0000)
-                    for d in (0, 1, -1):
-                        bb = np.uint32(int(b) + d * 0x10000)
-                        bf.add(float(np.array([bb], np.uint32).view(np.float32)[0]))
-                best = min(bf, key=lambda y: (abs(Fraction(y) - v),
-                                              (np.array([y], np.float32).view(np.uint32)[0] >> 16) & 1))
-                out[i, j] = best
-        return out
-
-    b1 = stage(aq[0], aq[1], *wq[0])
+    b1 = _exact_stage(aq[0], aq[1], *wq[0])
     np.testing.assert_array_equal(got["b1"], b1)
     a2 = [_brute_block(b1[r, 32 * c:32 * c + 32]) for r in range(m) for c in range(g1 // 32)]
     assert [int(x) for x in got["a2s"].ravel()] == [s for _, s in a2]
-    b2 = stage(got["a2"], got["a2s"], *wq[1])
+    assert [[int(x) for x in blk] for blk in got["a2"].reshape(-1, 32)] == [c for c, _ in a2]
+    b2 = _exact_stage(got["a2"], got["a2s"], *wq[1])
     np.testing.assert_array_equal(got["b2"], b2)
-    b3 = stage(got["a3"], got["a3s"], *wq[2])
+    a3 = [_brute_block(b2[r, 32 * c:32 * c + 32]) for r in range(m) for c in range(n2 // 32)]
+    assert [int(x) for x in got["a3s"].ravel()] == [s for _, s in a3]
+    assert [[int(x) for x in blk] for blk in got["a3"].reshape(-1, 32)] == [c for c, _ in a3]
+    b3 = _exact_stage(got["a3"], got["a3s"], *wq[2])
     np.testing.assert_array_equal(got["b3"], b3)
 
 
@@ -328,7 +344,7 @@ def test_rope_matches_float64_rotation_and_inverts():
 
 # ----------------------------------------------------------------------- WO-A
 def test_wo_a_tiny_brute_force():
-    t, g, h, r = 1, 2, 1, 16
+    t, g, h, r = 1, 2, 2, 16  # two heads per group: the group takes contiguous heads
     x = synth.bf16_bits_to_f64(synth.normal_bf16(9, 1, (t, g * h, 512)))
     pos = np.array([12345], np.int64)
     cs = synth.rope_cos_sin_cache(65536)
@@ -357,8 +373,10 @@ def test_wo_a_tiny_brute_force():
                                   wc[gg * r:(gg + 1) * r], ws[gg * r:(gg + 1) * r])
         for j in range(r):
             assert abs(Fraction(float(got["z"][0, gg * r + j])) - ex[0][j]) <= abs(ex[0][j]) * Fraction(2) ** -40 + Fraction(2) ** -200
-    qc, qs = oracle.mx_quantize(got["zb"])
-    np.testing.assert_array_equal(got["q"], qc)
+            assert got["zb"][0, gg * r + j] == _nearest_bf16(ex[0][j])
+    codes, scales = _brute_requant(got["zb"], g * r)
+    assert _blocks(got["q"]) == codes
+    assert [int(x) for x in got["qs"].ravel()] == scales
 
 
 # ------------------------------------------------------------ RMS norm split
@@ -396,3 +414,67 @@ def test_split_qkv_and_norm_parts():
     q2, s2 = oracle.mx_quantize(sp["y"])
     np.testing.assert_array_equal(sp["q"], q2)
     np.testing.assert_array_equal(sp["qs"], s2)
+    # the norm runs over the first 1536 columns only: scaling or zeroing the kv
+    # columns changes nothing in y, q or qs
+    for kv in (out1[:, 1536:] * 64, np.zeros((3, 512))):
+        sp2 = oracle.split_qkv_and_norm(np.concatenate([out1[:, :1536], kv], axis=1), w, 1e-6)
+        for key in ("y", "q", "qs"):
+            np.testing.assert_array_equal(sp2[key], sp[key])
+    # with a unit weight and eps 0, each normalized row has unit mean square
+    # (up to the bf16 rounding of y, relative 2**-8 per element)
+    y1 = oracle.split_qkv_and_norm(out1, np.ones(1536), 0.0)["y"]
+    assert np.all(np.abs(np.mean(y1 * y1, axis=-1) - 1.0) <= 2.0 ** -7)
+
+
+def _decimal_rms_norm_bf16(row, weight, eps) -> np.ndarray:
+    """RMS norm of one row evaluated in 60-digit decimal arithmetic, each
+    element rounded once to the nearest bf16."""
+    getcontext().prec = 60
+    xs = [Decimal(Fraction(float(v)).numerator) / Decimal(Fraction(float(v)).denominator) for v in row]
+    ms = sum(x * x for x in xs) / len(xs)
+    inv = 1 / (ms + Decimal(eps)).sqrt()
+    out = []
+    for x, w in zip(xs, weight):
+        v = Fraction(x * inv * (Decimal(Fraction(float(w)).numerator) / Decimal(Fraction(float(w)).denominator)))
+        out.append(_nearest_bf16(v))
+    return np.array(out)
+
+
+def test_chain_norm_tiny_brute_force():
+    m, k1, n1, g1, n2, n3 = 2, 64, 96, 64, 64, 32
+    a = synth.bf16_bits_to_f64(synth.block_scaled_bf16(8, 1, m, k1, -4, 4))
+    ws = [synth.bf16_bits_to_f64(synth.block_scaled_bf16(8, 10 + i, n, kk, -6, 6))
+          for i, (n, kk) in enumerate([(n1, k1), (n2, g1), (n3, n2)])]
+    nw = synth.bf16_bits_to_f64(synth.norm_weight_bf16(8, g1))
+    aq = oracle.mx_quantize(a)
+    wq = [oracle.mx_quantize(w) for w in ws]
+    got = oracle.chain_norm(aq[0], aq[1], wq, nw, 1e-6, g1_cols=g1)
+    b1 = _exact_stage(aq[0], aq[1], *wq[0])
+    np.testing.assert_array_equal(got["b1"], b1)
+    np.testing.assert_array_equal(got["kv"], b1[:, g1:])
+    y = np.stack([_decimal_rms_norm_bf16(b1[r, :g1], nw, 1e-6) for r in range(m)])
+    np.testing.assert_array_equal(got["y"], y)
+    codes, scales = _brute_requant(y, g1)
+    assert _blocks(got["a2"]) == codes and [int(x) for x in got["a2s"].ravel()] == scales
+    b2 = _exact_stage(got["a2"], got["a2s"], *wq[1])
+    np.testing.assert_array_equal(got["b2"], b2)
+    codes, scales = _brute_requant(b2, n2)
+    assert _blocks(got["a3"]) == codes and [int(x) for x in got["a3s"].ravel()] == scales
+    np.testing.assert_array_equal(got["b3"], _exact_stage(got["a3"], got["a3s"], *wq[2]))
+
+
+def test_chain_norm_removes_the_input_scale():
+    """Scaling the layer input by 2**k scales G1's output by 2**k exactly; with
+    eps = 0 the norm divides it out again, so everything after it is unchanged."""
+    m, k1, n1, g1, n2, n3 = 3, 128, 256, 128, 128, 128
+    a = synth.bf16_bits_to_f64(synth.block_scaled_bf16(9, 1, m, k1, -2, 2))
+    wq = [oracle.mx_quantize(synth.bf16_bits_to_f64(synth.block_scaled_bf16(9, 10 + i, n, kk, -2, 2)))
+          for i, (n, kk) in enumerate([(n1, k1), (n2, g1), (n3, n2)])]
+    nw = synth.bf16_bits_to_f64(synth.norm_weight_bf16(9, g1))
+    ac, asb = oracle.mx_quantize(a)
+    base = oracle.chain_norm(ac, asb, wq, nw, 0.0, g1_cols=g1)
+    for k in (-5, 3, 9):
+        got = oracle.chain_norm(ac, (asb.astype(np.int64) + k).astype(np.uint8), wq, nw, 0.0, g1_cols=g1)
+        np.testing.assert_array_equal(got["b1"], np.ldexp(base["b1"], k))
+        for key in ("y", "a2", "a2s", "b2", "a3", "a3s", "b3"):
+            np.testing.assert_array_equal(got[key], base[key])

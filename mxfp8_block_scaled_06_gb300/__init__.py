@@ -3,7 +3,10 @@
 Argument marshalling only: every step runs in the CUDA kernels behind the C ABI
 declared in include/mx.h; PyTorch supplies device memory and the current
 stream. There is no fallback: if libmx.so is missing or the device is not a
-compute-capability 10.3 GPU, the calls raise.
+compute-capability 10.3 GPU, the calls raise. Since the C entry points see only
+plain pointers, each wrapper first checks every tensor's element type, size,
+layout and residency on the handle's GPU (TypeError / ValueError, nothing
+launched).
 
 Names and argument order follow the C entry points: mx_create, mx_scale_bytes,
 mx_quantize_rows, mx_gemm, mx_gemm_chain, wo_a_grouped, mx_device_status.
@@ -125,15 +128,104 @@ def _empty_u8(shape, device):
     return torch.empty(shape, dtype=torch.uint8, device=device)
 
 
+# The C entry points take plain pointers and cannot see what they point at, so
+# the binding checks each tensor before the call: element type, size (so no
+# kernel reads or writes past a tensor's end), layout, and that it lives on the
+# handle's GPU. Violations raise TypeError / ValueError and launch nothing.
+_CODES = _SCALES = _BF16 = None
+
+
+def _types():
+    """(codes, scales, bf16) element types, resolved once."""
+    global _CODES, _SCALES, _BF16
+    if _CODES is None:
+        import torch
+        _CODES = (torch.uint8, torch.float8_e4m3fn)
+        _SCALES = (torch.uint8,) + ((torch.float8_e8m0fnu,) if hasattr(torch, "float8_e8m0fnu") else ())
+        _BF16 = (torch.bfloat16,)
+    return _CODES, _SCALES, _BF16
+
+
+def _codes_types():
+    return _types()[0]
+
+
+def _scale_types():
+    return _types()[1]
+
+
+def _bf16_type():
+    return _types()[2]
+
+
+def _sbytes(rows: int, k: int) -> int:
+    """mx_scale_bytes without the library call: ceil128(rows) * ceil4(k / 32), 0 for bad k."""
+    if rows < 0 or k <= 0 or k % 32:
+        return 0
+    return (rows + 127) // 128 * 128 * ((k // 32 + 3) // 4 * 4)
+
+
+def _resident(h: Handle, **tensors) -> None:
+    """Every given tensor lives on the handle's GPU (checked after all the others,
+    so a host tensor is only ever rejected here)."""
+    for name, t in tensors.items():
+        if t is not None and (t.get_device() != h.device or not t.is_cuda):
+            raise ValueError(f"{name}: on {t.device}, the handle's device is cuda:{h.device}")
+
+
+def _flat(name: str, t, dtypes, numel: int):
+    """A contiguous buffer of one of dtypes holding at least numel elements."""
+    if t is None:
+        raise ValueError(f"{name}: a tensor is required")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected one of {dtypes}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, at least {numel} needed")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t
+
+
+def _matrix(name: str, t, dtypes, rows: int, cols: int, row_stride: bool = False):
+    """A 2-D tensor of one of dtypes with at least rows rows of exactly cols
+    elements; contiguous, or (row_stride) with unit column stride and any row stride."""
+    if t is None:
+        raise ValueError(f"{name}: a tensor is required")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected one of {dtypes}")
+    shape = t.shape
+    if len(shape) != 2 or shape[0] < rows or shape[1] != cols:
+        raise ValueError(f"{name}: shape {tuple(shape)}, expected [>= {rows}, {cols}]")
+    if row_stride:
+        st = t.stride()
+        if st[1] != 1 or st[0] < cols:
+            raise ValueError(f"{name}: layout {st} not supported")
+    elif not t.is_contiguous():
+        raise ValueError(f"{name}: layout {t.stride()} not supported")
+    return t
+
+
+def _weight(i, w, s):
+    if w is None or w.dim() != 2:
+        raise ValueError(f"weight {i}: a 2-D [N, K] tensor is required")
+    n, k = w.shape
+    _matrix(f"weight {i}", w, _codes_types(), n, k)
+    _flat(f"weight {i} scales", s, _scale_types(), _sbytes(n, k))
+    return n, k
+
+
 def mx_quantize_rows(h: Handle, x, q=None, scales=None, swizzled: bool = True, stream=None):
     """bf16 [M, K] (row stride x.stride(0)) -> (E4M3 codes uint8 [M, K], scale bytes)."""
     import torch
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    if x.dim() != 2:
+        raise ValueError("x: a 2-D [M, K] tensor is required")
     m, k = x.shape
-    if q is None:
-        q = _empty_u8((m, k), x.device)
-    if scales is None:
-        scales = _empty_u8((mx_scale_bytes(m, k),) if swizzled else (m, k // 32), x.device)
+    _matrix("x", x, (torch.bfloat16,), m, k, row_stride=True)
+    sbytes = _sbytes(m, k) if swizzled else m * (k // 32)
+    q = _empty_u8((m, k), x.device) if q is None else _matrix("q", q, _codes_types(), m, k)
+    shape = (sbytes,) if swizzled else (m, k // 32)
+    scales = _empty_u8(shape, x.device) if scales is None else _flat("scales", scales, _scale_types(), sbytes)
+    _resident(h, x=x, q=q, scales=scales)
     _check(load_library().mx_quantize_rows(h.ptr, m, k, _ptr(x), x.stride(0), _ptr(q),
                                            _ptr(scales), int(swizzled), _stream(stream)),
            "mx_quantize_rows")
@@ -142,12 +234,16 @@ def mx_quantize_rows(h: Handle, x, q=None, scales=None, swizzled: bool = True, s
 
 def mx_gemm(h: Handle, a, a_scales, w, w_scales, out=None, m: int | None = None,
             pdl: bool = False, stream=None):
-    """out[M, N] bf16 = dequant(a[M, K]) x dequant(w[N, K])^T."""
+    """out[M, N] bf16 = dequant(a[M, K]) x dequant(w[N, K])^T (M = a's rows unless m is given)."""
     import torch
+    n, k = _weight(0, w, w_scales)
     m = a.shape[0] if m is None else m
-    n, k = w.shape
+    _matrix("a", a, _codes_types(), m, k)
+    _flat("a_scales", a_scales, _scale_types(), _sbytes(m, k))
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=w.device)
+    _matrix("out", out, (torch.bfloat16,), m, n)
+    _resident(h, a=a, a_scales=a_scales, w=w, w_scales=w_scales, out=out)
     _check(load_library().mx_gemm(h.ptr, m, n, k, _ptr(a), _ptr(a_scales), _ptr(w), _ptr(w_scales),
                                   _ptr(out), MX_FLAG_PDL if pdl else 0, _stream(stream)), "mx_gemm")
     return out
@@ -158,14 +254,45 @@ def mx_gemm_bf16(h: Handle, x, w, w_scales, out=None, m: int | None = None, pdl:
     """out[M, N] bf16 = dequant(MXFP8(x[M, K])) x dequant(w[N, K])^T, x bf16 with its
     quantization inside the GEMM kernel (row stride x.stride(0))."""
     import torch
+    n, k = _weight(0, w, w_scales)
     m = x.shape[0] if m is None else m
-    n, k = w.shape
+    _matrix("x", x, (torch.bfloat16,), m, k, row_stride=True)
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=w.device)
+    _matrix("out", out, (torch.bfloat16,), m, n)
+    _resident(h, x=x, w=w, w_scales=w_scales, out=out)
     _check(load_library().mx_gemm_bf16(h.ptr, m, n, k, _ptr(x), x.stride(0), _ptr(w), _ptr(w_scales),
                                        _ptr(out), MX_FLAG_PDL if pdl else 0, _stream(stream)),
            "mx_gemm_bf16")
     return out
+
+
+def _chain_buffers(a1, a1_scales, weights, g1_cols, a2, a2_scales, a3, a3_scales, out):
+    """Checks and allocations shared by the two chain entry points."""
+    import torch
+    if len(weights) != 3:
+        raise ValueError("weights: three (w, w_scales) pairs are required")
+    (n1, k1), (n2, _), (n3, _) = (_weight(i, w, s) for i, (w, s) in enumerate(weights))
+    m = a1.shape[0]
+    dev = a1.device
+    _matrix("a1", a1, _codes_types(), m, k1)
+    _flat("a1_scales", a1_scales, _scale_types(), _sbytes(m, k1))
+    a2 = _empty_u8((m, g1_cols), dev) if a2 is None else _matrix("a2", a2, _codes_types(), m, g1_cols)
+    a2_scales = (_empty_u8((_sbytes(m, g1_cols),), dev) if a2_scales is None else
+                 _flat("a2_scales", a2_scales, _scale_types(), _sbytes(m, g1_cols)))
+    a3 = _empty_u8((m, n2), dev) if a3 is None else _matrix("a3", a3, _codes_types(), m, n2)
+    a3_scales = (_empty_u8((_sbytes(m, n2),), dev) if a3_scales is None else
+                 _flat("a3_scales", a3_scales, _scale_types(), _sbytes(m, n2)))
+    out = torch.empty((m, n3), dtype=torch.bfloat16, device=dev) if out is None else out
+    _matrix("out", out, (torch.bfloat16,), m, n3)
+    ws = (MxWeight * 3)(*[MxWeight(_ptr(w), _ptr(s), w.shape[0], w.shape[1]) for w, s in weights])
+    return m, dev, ws, (n1, n2, n3), a2, a2_scales, a3, a3_scales, out
+
+
+def _chain_resident(h: Handle, a1, a1_scales, weights, a2, a2_scales, a3, a3_scales, out):
+    _resident(h, a1=a1, a1_scales=a1_scales, a2=a2, a2_scales=a2_scales, a3=a3, a3_scales=a3_scales,
+              out=out, **{f"weight {i}": w for i, (w, _) in enumerate(weights)},
+              **{f"weight {i} scales": s for i, (_, s) in enumerate(weights)})
 
 
 def mx_gemm_chain(h: Handle, a1, a1_scales, weights, g1_cols: int = 1536, out=None,
@@ -174,17 +301,11 @@ def mx_gemm_chain(h: Handle, a1, a1_scales, weights, g1_cols: int = 1536, out=No
     """Three projections on one stream with PDL: G1 -> MXFP8 requant of its first
     g1_cols columns -> G2 -> requant -> G3. weights = [(w, w_scales)] * 3."""
     import torch
-    m = a1.shape[0]
-    dev = a1.device
-    ws = (MxWeight * 3)(*[MxWeight(_ptr(w), _ptr(s), w.shape[0], w.shape[1]) for w, s in weights])
-    n1, n2, n3 = (w.shape[0] for w, _ in weights)
-    a2 = _empty_u8((m, g1_cols), dev) if a2 is None else a2
-    a2_scales = _empty_u8((mx_scale_bytes(m, g1_cols),), dev) if a2_scales is None else a2_scales
-    a3 = _empty_u8((m, n2), dev) if a3 is None else a3
-    a3_scales = _empty_u8((mx_scale_bytes(m, n2),), dev) if a3_scales is None else a3_scales
-    out = torch.empty((m, n3), dtype=torch.bfloat16, device=dev) if out is None else out
+    m, dev, ws, (n1, n2, n3), a2, a2_scales, a3, a3_scales, out = _chain_buffers(
+        a1, a1_scales, weights, g1_cols, a2, a2_scales, a3, a3_scales, out)
     d1 = torch.empty((m, n1), dtype=torch.bfloat16, device=dev) if debug else None
     d2 = torch.empty((m, n2), dtype=torch.bfloat16, device=dev) if debug else None
+    _chain_resident(h, a1, a1_scales, weights, a2, a2_scales, a3, a3_scales, out)
     _check(load_library().mx_gemm_chain(h.ptr, m, _ptr(a1), _ptr(a1_scales), ws, g1_cols, _ptr(a2),
                                         _ptr(a2_scales), _ptr(a3), _ptr(a3_scales), _ptr(out),
                                         _ptr(d1), _ptr(d2), _stream(stream)), "mx_gemm_chain")
@@ -196,13 +317,17 @@ def mx_rmsnorm_quantize_rows(h: Handle, x, norm_weight, eps: float, q=None, scal
     """bf16 [M, K] (row stride x.stride(0)) -> RMS-normalized with norm_weight [K] bf16 and
     eps, rounded to bf16 (returned as y when asked) and MX-quantized: (q, scales, y)."""
     import torch
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    if x.dim() != 2:
+        raise ValueError("x: a 2-D [M, K] tensor is required")
     m, k = x.shape
-    if q is None:
-        q = _empty_u8((m, k), x.device)
-    if scales is None:
-        scales = _empty_u8((mx_scale_bytes(m, k),) if swizzled else (m, k // 32), x.device)
+    _matrix("x", x, (torch.bfloat16,), m, k, row_stride=True)
+    _flat("norm_weight", norm_weight, (torch.bfloat16,), k)
+    sbytes = _sbytes(m, k) if swizzled else m * (k // 32)
+    q = _empty_u8((m, k), x.device) if q is None else _matrix("q", q, _codes_types(), m, k)
+    shape = (sbytes,) if swizzled else (m, k // 32)
+    scales = _empty_u8(shape, x.device) if scales is None else _flat("scales", scales, _scale_types(), sbytes)
     yt = torch.empty((m, k), dtype=torch.bfloat16, device=x.device) if y else None
+    _resident(h, x=x, norm_weight=norm_weight, q=q, scales=scales)
     _check(load_library().mx_rmsnorm_quantize_rows(h.ptr, m, k, _ptr(x), x.stride(0),
                                                    _ptr(norm_weight), float(eps), _ptr(yt), _ptr(q),
                                                    _ptr(scales), int(swizzled), _stream(stream)),
@@ -216,18 +341,15 @@ def mx_gemm_chain_norm(h: Handle, a1, a1_scales, weights, norm_weight, eps: floa
     """mx_gemm_chain with the RMS-norm split between G1 and G2: G1's bf16 output goes
     to out1 (qr | kv), qr is normalized and quantized for G2."""
     import torch
-    m = a1.shape[0]
-    dev = a1.device
-    ws = (MxWeight * 3)(*[MxWeight(_ptr(w), _ptr(s), w.shape[0], w.shape[1]) for w, s in weights])
-    n1, n2, n3 = (w.shape[0] for w, _ in weights)
+    m, dev, ws, (n1, n2, n3), a2, a2_scales, a3, a3_scales, out = _chain_buffers(
+        a1, a1_scales, weights, g1_cols, a2, a2_scales, a3, a3_scales, out)
+    _flat("norm_weight", norm_weight, (torch.bfloat16,), g1_cols)
     out1 = torch.empty((m, n1), dtype=torch.bfloat16, device=dev) if out1 is None else out1
-    a2 = _empty_u8((m, g1_cols), dev) if a2 is None else a2
-    a2_scales = _empty_u8((mx_scale_bytes(m, g1_cols),), dev) if a2_scales is None else a2_scales
-    a3 = _empty_u8((m, n2), dev) if a3 is None else a3
-    a3_scales = _empty_u8((mx_scale_bytes(m, n2),), dev) if a3_scales is None else a3_scales
-    out = torch.empty((m, n3), dtype=torch.bfloat16, device=dev) if out is None else out
+    _matrix("out1", out1, (torch.bfloat16,), m, n1)
     dy = torch.empty((m, g1_cols), dtype=torch.bfloat16, device=dev) if debug else None
     d2 = torch.empty((m, n2), dtype=torch.bfloat16, device=dev) if debug else None
+    _chain_resident(h, a1, a1_scales, weights, a2, a2_scales, a3, a3_scales, out)
+    _resident(h, norm_weight=norm_weight, out1=out1)
     _check(load_library().mx_gemm_chain_norm(h.ptr, m, _ptr(a1), _ptr(a1_scales), ws, g1_cols,
                                              _ptr(norm_weight), float(eps), _ptr(out1), _ptr(a2),
                                              _ptr(a2_scales), _ptr(a3), _ptr(a3_scales), _ptr(out),
@@ -237,6 +359,33 @@ def mx_gemm_chain_norm(h: Handle, a1, a1_scales, weights, norm_weight, eps: floa
                 out2=d2)
 
 
+def _wo_a_inputs(x, positions, cos_sin, w, w_scales, n_groups, heads_per_group,
+                 o_lora_rank, d_nope, d_rope):
+    """Checks shared by the two WO-A entry points; returns (T, K of all groups, columns)."""
+    import torch
+    t = x.shape[0]
+    kall = n_groups * heads_per_group * (d_nope + d_rope)
+    cols = n_groups * o_lora_rank
+    if x.dtype != torch.bfloat16:
+        raise TypeError(f"x: dtype {x.dtype}, expected torch.bfloat16")
+    # each token's heads x dims are contiguous; tokens are x.stride(0) elements apart
+    if x.dim() < 2 or x.stride(-1) != 1 or not x[0].is_contiguous() or x[0].numel() != kall:
+        raise ValueError(f"x: each token must hold {kall} contiguous elements")
+    if x.stride(0) < kall:
+        raise ValueError(f"x: token stride {x.stride(0)} below {kall}")
+    _flat("positions", positions, (torch.int64,), t)
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != d_rope:
+        raise ValueError(f"cos_sin: shape {tuple(cos_sin.shape)}, expected [max_pos, {d_rope}]")
+    _flat("cos_sin", cos_sin, (torch.float32,), 0)
+    _matrix("w", w, _codes_types(), cols, heads_per_group * (d_nope + d_rope))
+    _flat("w_scales", w_scales, _scale_types(), _sbytes(cols, heads_per_group * (d_nope + d_rope)))
+    return t, kall, cols
+
+
+def _wo_a_resident(h: Handle, x, positions, cos_sin, w, w_scales):
+    _resident(h, x=x, positions=positions, cos_sin=cos_sin, w=w, w_scales=w_scales)
+
+
 def wo_a_grouped(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,
                  heads_per_group: int, o_lora_rank: int, d_nope: int = 448, d_rope: int = 64,
                  q=None, q_scales=None, debug: bool = False, early_trigger: bool = False,
@@ -244,15 +393,17 @@ def wo_a_grouped(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,
     """x: bf16 [T, heads, d_nope + d_rope] (token stride x.stride(0)); returns the
     MXFP8 activation (q, q_scales) for wo_b, plus debug tensors if asked."""
     import torch
-    t = x.shape[0]
+    t, kall, cols = _wo_a_inputs(x, positions, cos_sin, w, w_scales, n_groups, heads_per_group,
+                                 o_lora_rank, d_nope, d_rope)
     dev = x.device
-    cols = n_groups * o_lora_rank
-    kall = n_groups * heads_per_group * (d_nope + d_rope)
-    q = _empty_u8((t, cols), dev) if q is None else q
-    q_scales = _empty_u8((mx_scale_bytes(t, cols),), dev) if q_scales is None else q_scales
+    q = _empty_u8((t, cols), dev) if q is None else _matrix("q", q, _codes_types(), t, cols)
+    q_scales = (_empty_u8((_sbytes(t, cols),), dev) if q_scales is None else
+                _flat("q_scales", q_scales, _scale_types(), _sbytes(t, cols)))
     dz = torch.empty((t, cols), dtype=torch.bfloat16, device=dev) if debug else None
     dxq = _empty_u8((t, kall), dev) if debug else None
     dxs = _empty_u8((t, kall // 32), dev) if debug else None
+    _wo_a_resident(h, x, positions, cos_sin, w, w_scales)
+    _resident(h, q=q, q_scales=q_scales)
     _check(load_library().wo_a_grouped(h.ptr, t, _ptr(x), x.stride(0), _ptr(positions),
                                        _ptr(cos_sin), cos_sin.shape[0], _ptr(w), _ptr(w_scales),
                                        n_groups, heads_per_group, d_nope, d_rope, o_lora_rank,
@@ -268,15 +419,18 @@ def wo_a_grouped_unfused(h: Handle, x, positions, cos_sin, w, w_scales, n_groups
     """wo_a_grouped in two launches (RoPE + quantize into the caller-owned xq, then a
     grouped GEMM with the requantization fused); for token counts up to 256."""
     import torch
-    t = x.shape[0]
+    t, kall, cols = _wo_a_inputs(x, positions, cos_sin, w, w_scales, n_groups, heads_per_group,
+                                 o_lora_rank, d_nope, d_rope)
     dev = x.device
-    cols = n_groups * o_lora_rank
-    kall = n_groups * heads_per_group * (d_nope + d_rope)
-    q = _empty_u8((t, cols), dev) if q is None else q
-    q_scales = _empty_u8((mx_scale_bytes(t, cols),), dev) if q_scales is None else q_scales
-    xq = _empty_u8((t, kall), dev) if xq is None else xq
-    xq_scales = _empty_u8((mx_scale_bytes(t, kall),), dev) if xq_scales is None else xq_scales
+    q = _empty_u8((t, cols), dev) if q is None else _matrix("q", q, _codes_types(), t, cols)
+    q_scales = (_empty_u8((_sbytes(t, cols),), dev) if q_scales is None else
+                _flat("q_scales", q_scales, _scale_types(), _sbytes(t, cols)))
+    xq = _empty_u8((t, kall), dev) if xq is None else _matrix("xq", xq, _codes_types(), t, kall)
+    xq_scales = (_empty_u8((_sbytes(t, kall),), dev) if xq_scales is None else
+                 _flat("xq_scales", xq_scales, _scale_types(), _sbytes(t, kall)))
     zt = torch.empty((t, cols), dtype=torch.bfloat16, device=dev) if z else None
+    _wo_a_resident(h, x, positions, cos_sin, w, w_scales)
+    _resident(h, q=q, q_scales=q_scales, xq=xq, xq_scales=xq_scales)
     _check(load_library().wo_a_grouped_unfused(h.ptr, t, _ptr(x), x.stride(0), _ptr(positions),
                                                _ptr(cos_sin), cos_sin.shape[0], _ptr(w),
                                                _ptr(w_scales), n_groups, heads_per_group, d_nope,

@@ -115,8 +115,9 @@ def test_wo_a_rejects_unsupported_shapes():
     (wq, wsc), _, _, cs_dev = _setup()
     x = torch.zeros((4, G * H, D), dtype=torch.bfloat16, device="cuda")
     pos = torch.zeros(4, dtype=torch.int64, device="cuda")
+    cs128 = torch.zeros((1024, 128), dtype=torch.float32, device="cuda")  # a cache matching d_rope
     with pytest.raises(mx.MxError) as e:
-        mx.wo_a_grouped(handle(), x, pos, cs_dev, wq, wsc, G, H, R, d_nope=384, d_rope=128)
+        mx.wo_a_grouped(handle(), x, pos, cs128, wq, wsc, G, H, R, d_nope=384, d_rope=128)
     assert e.value.code == mx.MX_ERR_UNSUPPORTED
     x129 = torch.zeros((129, G * H, D), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mx.MxError) as e:

@@ -106,6 +106,6 @@ def test_unfused_rejects_unsupported():
     assert e.value.code == mx.MX_ERR_UNSUPPORTED
     x4 = torch.zeros((4, G * H, D), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mx.MxError) as e:
-        mx.wo_a_grouped_unfused(handle(), x4, pos[:4], cs_dev, wq, wsc, G, H, R, d_nope=384,
-                                d_rope=128)
+        mx.wo_a_grouped_unfused(handle(), x4, pos[:4], torch.zeros((1024, 128), device="cuda"), wq, wsc,
+                                G, H, R, d_nope=384, d_rope=128)
     assert e.value.code == mx.MX_ERR_UNSUPPORTED

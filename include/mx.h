@@ -228,6 +228,16 @@ int wo_a_grouped_unfused(mx_handle* h, int T, const void* x, long ldx,
  * gave up on a bounded wait since the last call. Synchronizes the device. */
 int mx_device_status(mx_handle* h, int* status);
 
+/* Diagnostic of the failure path. Launches one thread that waits, through the
+ * bounded mbarrier wait every kernel's pipeline uses, on a barrier that nothing
+ * completes. After the wait's limit (one second of the GPU's global timer) the
+ * thread records a timeout in the handle's status word and the kernel returns,
+ * so the next mx_device_status reports MX_ERR_TIMEOUT and the context stays
+ * usable: a wait that cannot complete ends as a status, not as a hung GPU.
+ * Asynchronous on stream; returns MX_OK once launched, MX_ERR_INVALID_ARG for a
+ * null handle, MX_ERR_DEVICE if another device is current. */
+int mx_wait_selftest(mx_handle* h, void* stream);
+
 /* Human-readable name of a status code. */
 const char* mx_status_string(int status);
 

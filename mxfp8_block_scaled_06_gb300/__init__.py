@@ -25,7 +25,7 @@ MX_FLAG_PDL = 1
 EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows",
            "mx_rmsnorm_quantize_rows", "mx_gemm", "mx_gemm_bf16", "mx_gemm_chain",
            "mx_gemm_chain_norm", "wo_a_grouped", "wo_a_grouped_unfused", "mx_device_status",
-           "mx_status_string"]
+           "mx_wait_selftest", "mx_status_string"]
 
 _vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
 
@@ -69,6 +69,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.wo_a_grouped_unfused.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i,
                                          _i, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.mx_device_status.argtypes = [_vp, ctypes.POINTER(_i)]
+    lib.mx_wait_selftest.argtypes = [_vp, _vp]
     lib.mx_status_string.argtypes = [_i]
     lib.mx_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -445,3 +446,10 @@ def mx_device_status(h: Handle) -> int:
     v = _i(0)
     _check(load_library().mx_device_status(h.ptr, ctypes.byref(v)), "mx_device_status")
     return v.value
+
+
+def mx_wait_selftest(h: Handle, stream=None) -> None:
+    """Launch the bounded-wait diagnostic: about one second later the kernel gives
+    up on a barrier nothing completes, and the next mx_device_status reports
+    MX_ERR_TIMEOUT."""
+    _check(load_library().mx_wait_selftest(h.ptr, _stream(stream)), "mx_wait_selftest")

@@ -402,6 +402,12 @@ int mx_device_status(mx_handle* h, int* status) {
   return MX_OK;
 }
 
+int mx_wait_selftest(mx_handle* h, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  return cuda_status(mx::launch_wait_selftest(h->d_status, static_cast<cudaStream_t>(stream)));
+}
+
 const char* mx_status_string(int s) {
   switch (s) {
     case MX_OK: return "MX_OK";

@@ -29,6 +29,10 @@ cudaError_t launch_rmsnorm_quantize_rows(const void* x, long ldx, int M, int K, 
                                          float eps, void* y, void* q, void* scales, int swizzled,
                                          cudaStream_t stream);
 
+// One thread waits on an mbarrier nothing completes; after the bounded wait's
+// limit it sets the timeout bit of *status and returns.
+cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);
+
 // ------------------------------------------------------------ block-scaled GEMM
 // Plan of one GEMM launch: activation tile (MMA N), K-splits per weight tile
 // (a thread-block cluster along K), pipeline depth, TMEM columns, shared bytes.

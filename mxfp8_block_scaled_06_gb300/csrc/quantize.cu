@@ -262,4 +262,22 @@ cudaError_t launch_quantize_rows(const void* x, long ldx, int M, int K, void* q,
                             rows_total, groups_per_row, rope);
 }
 
+// ------------------------------------------------------------ wait self-test
+// One thread waits, through the same bounded mbar_wait the kernels use, on an
+// mbarrier that nothing ever arrives on. The wait gives up after kWaitLimitNs,
+// the thread records kStatusTimeout and the kernel returns: the failure path of
+// every pipeline wait, taken on purpose and without a fault. Nothing is in
+// flight on the barrier, so it is simply abandoned at exit.
+__global__ void wait_selftest_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  if (!mbar_wait(b, 0)) atomicOr(status, kStatusTimeout);
+}
+
+cudaError_t launch_wait_selftest(int* status, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 1, 0, stream>>>(status);
+  return cudaGetLastError();
+}
+
 }  // namespace mx

@@ -86,6 +86,7 @@ def test_null_handle_is_rejected_before_any_device_call(lib):
                              None, None) == mx.MX_ERR_INVALID_ARG
     assert lib.wo_a_grouped(None, 1, None, 0, None, None, 1, None, None, 4, 8, 448, 64, 1024, None,
                             None, None, None, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_wait_selftest(None, None) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_destroy(None) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_create(None, 0) == mx.MX_ERR_INVALID_ARG
 

@@ -69,7 +69,7 @@ def test_chain_equals_composition_small(m):
     _composition(m, [(384, 640), (256, 256), (512, 256)], 256, seed=7)
 
 
-@pytest.mark.parametrize("m", [1, 8, 64])
+@pytest.mark.parametrize("m", [1, 8, 64, 129, 256])
 def test_chain_equals_composition_decode_shapes(m):
     _composition(m, [(2048, 5120), (8192, 1536), (5120, 8192)], 1536, seed=2)
 

@@ -60,8 +60,9 @@ def test_bf16_ragged_rows_and_row_batches(m):
     _run(m, 384, 640, seed=20 + m)
 
 
-def test_bf16_two_activation_row_tiles():
-    _run(130, 256, 512, seed=3)
+@pytest.mark.parametrize("m", [130, 256])
+def test_bf16_two_activation_row_tiles(m):
+    _run(m, 256, 512, seed=3)
 
 
 @pytest.mark.parametrize("n,k", [(128, 128), (1024, 128), (640, 4096), (8192, 1536)])

@@ -44,6 +44,19 @@ def test_quantize_weight_full_size():
     _check(synth.block_scaled_bf16(1, synth.TAG_W, 2048, 5120, -6, 6))
 
 
+def test_quantize_max_rows():
+    # the largest row count the entry point takes, and one more
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    _check(synth.block_scaled_bf16(5, 12, 65536, 64, -6, 6))
+    x = torch.zeros((2, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((2, 64), dtype=torch.uint8, device="cuda")
+    s = torch.zeros(mx.mx_scale_bytes(2, 64), dtype=torch.uint8, device="cuda")
+    rc = mx.load_library().mx_quantize_rows(handle().ptr, 65537, 64, x.data_ptr(), 64, q.data_ptr(),
+                                            s.data_ptr(), 1, None)
+    assert rc == mx.MX_ERR_INVALID_ARG
+
+
 def test_quantize_strided_rows():
     _check(synth.block_scaled_bf16(3, 9, 5, 512, -4, 4), ldx=512 + 64)
 

@@ -218,11 +218,6 @@ def mx_gemm_exact(a_codes, a_sbytes, w_codes, w_sbytes) -> list[list[Fraction]]:
     return [[sum(fa[i][j] * fw[c][j] for j in range(k)) for c in range(n)] for i in range(m)]
 
 
-def mx_gemm_rows(a_codes, a_sbytes, w_codes_rows, w_sbytes_rows) -> np.ndarray:
-    """Sampled outputs: the GEMM against a subset of weight rows (columns of out)."""
-    return mx_gemm(a_codes, a_sbytes, w_codes_rows, w_sbytes_rows)
-
-
 # ----------------------------------------------------------------------------
 # Three-projection chain (fused_wqa_wkv -> wq_b -> wo_b of the decode step)
 # ----------------------------------------------------------------------------

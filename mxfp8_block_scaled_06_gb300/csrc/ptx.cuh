@@ -34,9 +34,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -103,11 +100,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ------------------------------------------------------------------ cluster
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
@@ -215,19 +207,9 @@ __device__ __forceinline__ uint32_t idesc_mxf8(uint32_t n, uint32_t sf_id) {
          ((128u >> 4) << 24) | (sf_id << 29);
 }
 // D[tmem] (+)= A[smem] x B[smem]^T with per-32 scales from TMEM.
-__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], "
-      "[%6], p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
-}
-// The same MMA with each smem descriptor passed as its two 32-bit halves: a
-// loop that walks a ring only changes the low half (the address field), so it
-// advances descriptors with 32-bit adds and keeps the high halves in registers.
+// Each shared-memory descriptor is passed as its two 32-bit halves: a loop that
+// walks a ring only changes the low half (the address field), so it advances
+// descriptors with 32-bit adds and keeps the high halves in registers.
 __device__ __forceinline__ void mma_mxf8_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                             uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                             uint32_t sfa_tmem, uint32_t sfb_tmem,
@@ -242,16 +224,12 @@ __device__ __forceinline__ void mma_mxf8_lh(uint32_t d_tmem, uint32_t a_lo, uint
       "r"(sfb_tmem)
       : "memory");
 }
+// Copy a 32x128-bit smem tile into TMEM lanes 0-31, replicated into all four
+// 32-lane quarters (4 columns); the descriptor as its two 32-bit halves.
 __device__ __forceinline__ void tmem_cp_32x128b_x4_lh(uint32_t taddr, uint32_t lo, uint32_t hi) {
   asm volatile("{\n\t.reg .b64 d;\n\tmov.b64 d, {%1, %2};\n\t"
                "tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], d;\n\t}" ::"r"(taddr),
                "r"(lo), "r"(hi)
-               : "memory");
-}
-// Copy a 32x128-bit smem tile into TMEM lanes 0-31, replicated into all four
-// 32-lane quarters (4 columns).
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
 }
 // Each thread of the warp reads 16 consecutive 32-bit columns of its TMEM lane.

@@ -107,3 +107,44 @@ def test_wo_a_guards(t):
                             xq_scales=xqs)
     g.check()
     assert mx.mx_device_status(handle()) == mx.MX_OK
+
+
+def test_empty_inputs_are_rejected_and_launch_nothing():
+    """Zero rows or tokens: every entry point returns MX_ERR_INVALID_ARG before
+    any launch (the documented domain starts at one row), and no output byte
+    changes."""
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    lib, h = mx.load_library(), handle().ptr
+    g = Guarded()
+    k, n = 512, 256
+    x = bf16_to_device(synth.block_scaled_bf16(6, synth.TAG_A, 4, k, -4, 4))
+    nw = torch.ones(k, dtype=torch.bfloat16, device="cuda")
+    wq, wsc = quantize_on_gpu(synth.block_scaled_bf16(6, synth.TAG_W, n, k, -6, 6))
+    aq, asc = quantize_on_gpu(synth.block_scaled_bf16(6, synth.TAG_A, 4, k, -6, 6))
+    q, s, out = g.u8(4 * k), g.u8(mx.mx_scale_bytes(4, k)), g.u8(4 * n * 2)
+    p = lambda t: t.data_ptr()
+    err = mx.MX_ERR_INVALID_ARG
+    assert lib.mx_quantize_rows(h, 0, k, p(x), k, p(q), p(s), 1, None) == err
+    assert lib.mx_rmsnorm_quantize_rows(h, 0, k, p(x), k, p(nw), 1e-6, None, p(q), p(s), 1, None) == err
+    assert lib.mx_gemm(h, 0, n, k, p(aq), p(asc), p(wq), p(wsc), p(out), 0, None) == err
+    assert lib.mx_gemm_bf16(h, 0, n, k, p(x), k, p(wq), p(wsc), p(out), 0, None) == err
+    # three [256, 512] weights: the row count is checked first
+    ws = (mx.MxWeight * 3)(*[mx.MxWeight(p(wq), p(wsc), n, k)] * 3)
+    assert lib.mx_gemm_chain(h, 0, p(aq), p(asc), ws, 512, p(q), p(s), p(q), p(s), p(out),
+                             None, None, None) == err
+    assert lib.mx_gemm_chain_norm(h, 0, p(aq), p(asc), ws, 512, p(nw), 1e-6, p(out), p(q), p(s),
+                                  p(q), p(s), p(out), None, None, None) == err
+    G, H, R, D = 4, 8, 1024, 512
+    ww = quantize_on_gpu(synth.block_scaled_bf16(6, synth.TAG_WOA, G * R, H * D, -6, 6))
+    cs = torch.zeros((16, 64), dtype=torch.float32, device="cuda")
+    xt = torch.zeros((1, G * H, D), dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(1, dtype=torch.int64, device="cuda")
+    assert lib.wo_a_grouped(h, 0, p(xt), G * H * D, p(pos), p(cs), 16, p(ww[0]), p(ww[1]), G, H, 448,
+                            64, R, p(q), p(s), None, None, None, 0, None) == err
+    assert lib.wo_a_grouped_unfused(h, 0, p(xt), G * H * D, p(pos), p(cs), 16, p(ww[0]), p(ww[1]), G,
+                                    H, 448, 64, R, p(q), p(s), None, p(q), p(s), None) == err
+    g.check()
+    for buf, nbytes in g.bufs:  # the outputs themselves are untouched too
+        assert (buf[PAD:PAD + nbytes].cpu().numpy() == PATTERN).all()
+    assert mx.mx_device_status(handle()) == mx.MX_OK

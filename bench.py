@@ -13,6 +13,7 @@ bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --profile gemm|chain|wo_a|sweep   (a few plain launches for ncu)
+  python bench.py --timeline   (per-CTA phase timeline, timeline build of the library)
 """
 from __future__ import annotations
 
@@ -605,6 +606,116 @@ def run_profile(args):
     print(json.dumps({"profile": args.profile, "ok": True}))
 
 
+TIMELINE_SLOTS = ("entry", "setup", "w_issued", "wsf_landed", "wait_ret", "first_full", "accum",
+                  "red_pass", "red_done", "exit")
+
+
+def run_timeline(args):
+    """--timeline: per-CTA %globaltimer stamps of GEMM launches (the timeline
+    build of libmx, -DMX_TIMELINE) in CUDA graphs of back-to-back launches with
+    PDL. For every launch after the first, each phase is reported relative to the
+    previous launch's last CTA exit (median and range over the launch's CTAs,
+    then the median over launches); the weights rotate over >= 3x L2."""
+    import ctypes
+
+    import torch
+
+    import mxfp8_block_scaled_06_gb300 as mx
+    from mxfp8_block_scaled_06_gb300 import build as mxbuild
+
+    lib = mx.load_library(mxbuild.build_timeline())
+    lib.mx_timeline_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                     ctypes.POINTER(ctypes.c_int)]
+    lib.mx_timeline_reset.argtypes = [ctypes.c_void_p]
+    ctas, slots, launches = 512, 12, 256
+    torch.cuda.set_device(0)
+    h = mx.mx_create(0)
+    props = torch.cuda.get_device_properties(0)
+    rig = Rig(torch, mx, h, getattr(props, "L2_cache_size", 126 * 2**20))
+    stream = torch.cuda.Stream()
+
+    def record(fn, per_graph):
+        with torch.cuda.stream(stream):
+            fn(0)  # tensor maps and plans outside the capture
+        torch.cuda.synchronize()
+        assert lib.mx_timeline_reset(h.ptr) == 0  # slots from here on belong to the captured launches
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(per_graph):
+                    fn(i)
+        torch.cuda.synchronize()
+        st, sp = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            st.record(stream)
+            for _ in range(5):
+                g.replay()
+            sp.record(stream)
+        sp.synchronize()
+        ms = st.elapsed_time(sp)
+        n = ctypes.c_int(0)
+        buf = np.zeros(launches * ctas * slots, dtype=np.uint64)
+        assert lib.mx_timeline_read(h.ptr, buf.ctypes.data, buf.nbytes, ctypes.byref(n)) == 0
+        tl = buf.reshape(launches, ctas, slots)[: n.value]
+        phases = {k: [] for k in TIMELINE_SLOTS}
+        dur, early, landed_early = [], [], []
+        for i in range(1, len(tl)):
+            prev = tl[i - 1][tl[i - 1][:, 9] > 0]
+            cur = tl[i][tl[i][:, 9] > 0]
+            if len(prev) == 0 or len(cur) == 0:
+                continue
+            p_end = int(prev[:, 9].max())
+            rel = cur[:, :10].astype(np.int64) - p_end
+            dur.append((int(cur[:, 9].max()) - p_end) / 1e3)
+            early.append(float((rel[:, 0] < 0).mean()))
+            landed_early.append(float(((rel[:, 3] < 0) & (cur[:, 3] > 0)).mean()))
+            for j, k in enumerate(TIMELINE_SLOTS):
+                v = rel[:, j][cur[:, j] > 0]
+                if len(v):
+                    phases[k].append(float(np.median(v)))
+        return {"us_per_graph_item": round(ms * 1e3 / (5 * per_graph), 3),
+                "launch_us_median": round(float(np.median(dur)), 3) if dur else None,
+                "ctas_started_before_previous_end": round(float(np.median(early)), 3) if early else None,
+                "weight_scales_landed_before_previous_end": round(float(np.median(landed_early)), 3)
+                if landed_early else None,
+                "phase_ns_vs_previous_end": {k: int(np.median(v)) for k, v in phases.items() if v}}
+
+    out = {}
+    nset = rig.copies(w_bytes(N1, K1))
+    wts = rig.weight_set([(N1, K1)], seed=1, ncopies=nset)
+    for m in (1, 8):
+        q = mx.mx_quantize_rows(h, rig.activation(m, K1, seed=1))
+        o = torch.empty((m, N1), dtype=torch.bfloat16, device=rig.dev)
+        out[f"gemm_M{m}"] = record(lambda i, q=q, o=o: mx.mx_gemm(
+            h, q[0], q[1], *wts[i % nset][0], out=o, pdl=True, stream=stream), 12)
+    xs = {m: rig.activation(m, K1, seed=1) for m in M_LIST}
+    qa = {m: mx.mx_quantize_rows(h, xs[m]) for m in M_LIST}
+    outs = {m: torch.empty((m, N1), dtype=torch.bfloat16, device=rig.dev) for m in M_LIST}
+
+    def step(i):
+        for j, m in enumerate(M_LIST):
+            mx.mx_quantize_rows(h, xs[m], q=qa[m][0], scales=qa[m][1], stream=stream)
+            mx.mx_gemm(h, qa[m][0], qa[m][1], *wts[(i * len(M_LIST) + j) % nset][0], out=outs[m],
+                       pdl=True, stream=stream)
+    out["step"] = record(step, 3)
+    cset = rig.copies(sum(w_bytes(n, k) for n, k in CHAIN_SHAPES))
+    cw = rig.weight_set(CHAIN_SHAPES, seed=2, ncopies=cset)
+    for m in (1, 16, 64):
+        q1 = mx.mx_quantize_rows(h, rig.activation(m, CHAIN_SHAPES[0][1], seed=2, umin=-4, umax=4))
+        bufs = dict(out=torch.empty((m, CHAIN_SHAPES[2][0]), dtype=torch.bfloat16, device=rig.dev),
+                    a2=torch.empty((m, CHAIN_G1_COLS), dtype=torch.uint8, device=rig.dev),
+                    a2_scales=torch.empty(mx.mx_scale_bytes(m, CHAIN_G1_COLS), dtype=torch.uint8, device=rig.dev),
+                    a3=torch.empty((m, CHAIN_SHAPES[1][0]), dtype=torch.uint8, device=rig.dev),
+                    a3_scales=torch.empty(mx.mx_scale_bytes(m, CHAIN_SHAPES[1][0]), dtype=torch.uint8,
+                                          device=rig.dev))
+        out[f"chain_M{m}"] = record(lambda i, q1=q1, bufs=bufs: mx.mx_gemm_chain(
+            h, q1[0], q1[1], cw[i % cset], g1_cols=CHAIN_G1_COLS, stream=stream, **bufs), 4)
+    torch.cuda.synchronize()
+    assert mx.mx_device_status(h) == mx.MX_OK
+    print(json.dumps({"timeline": out}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,7 +729,12 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMM launch from an ncu capture of the current kernel")
     ap.add_argument("--profile", default=None, choices=["gemm", "chain", "wo_a", "sweep"])
+    ap.add_argument("--timeline", action="store_true",
+                    help="per-CTA phase timeline of GEMM launches (builds the -DMX_TIMELINE library)")
     args = ap.parse_args()
+    if args.timeline:
+        run_timeline(args)
+        return
     if args.profile:
         run_profile(args)
         return

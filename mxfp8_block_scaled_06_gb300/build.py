@@ -14,6 +14,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmx.so")
+# Timeline build: the same sources with -DMX_TIMELINE (per-CTA %globaltimer
+# stamps of every GEMM launch, read back with mx_timeline_read); diagnostic only.
+TIMELINE_LIB = os.path.join(HERE, "libmx_timeline.so")
+TIMELINE_BUILD = os.path.join(HERE, "_build_timeline")
 SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "wo_a.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -36,14 +40,18 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(verbose: bool = False, force: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra: list[str] | None = None,
+          lib: str = LIB, build_dir: str = BUILD) -> str:
+    """Compile the sources (in parallel) and link `lib`; objects go to build_dir.
+    `extra` adds nvcc flags (e.g. -DMX_TIMELINE for the timeline build, which
+    needs its own lib and build_dir)."""
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, s):
             cmd = [cc, *ARCH, *FLAGS, *(extra or []), "-c", s, "-o", o]
@@ -60,14 +68,18 @@ def build(verbose: bool = False, force: bool = False, extra: list[str] | None = 
             print(text, file=sys.stderr)
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    if force or procs or not os.path.exists(LIB):
-        tmp = LIB + ".tmp"
+    if force or procs or not os.path.exists(lib):
+        tmp = lib + ".tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build_timeline(verbose: bool = False) -> str:
+    return build(verbose=verbose, extra=["-DMX_TIMELINE"], lib=TIMELINE_LIB, build_dir=TIMELINE_BUILD)
 
 
 if __name__ == "__main__":

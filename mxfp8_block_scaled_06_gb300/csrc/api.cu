@@ -2,6 +2,7 @@
 // validation (always before any launch), launch plans, TMA tensor maps.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <new>
@@ -30,7 +31,16 @@ struct mx_handle {
   TmapEntry tmaps[kTmapCache];
   int tmap_count;
   int tmap_next;  // round-robin replacement
+#ifdef MX_TIMELINE
+  unsigned long long* d_tl;  // kTimelineLaunches x kTimelineCtas x kTimelineSlots stamps
+  int tl_next;               // GEMM launches recorded since the last reset
+#endif
 };
+#ifdef MX_TIMELINE
+constexpr int kTimelineLaunches = 256;
+constexpr size_t kTimelineBytes =
+    sizeof(unsigned long long) * kTimelineLaunches * mx::kTimelineCtas * mx::kTimelineSlots;
+#endif
 
 namespace {
 
@@ -120,6 +130,11 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
   args.q_scales = q_scales;
   args.q_cols = q_cols;
   args.status = h->d_status;
+#ifdef MX_TIMELINE
+  args.tl = nullptr;
+  if (h->d_tl != nullptr && (N / 128) * plan.splits <= mx::kTimelineCtas && h->tl_next < kTimelineLaunches)
+    args.tl = h->d_tl + static_cast<size_t>(h->tl_next++) * mx::kTimelineCtas * mx::kTimelineSlots;
+#endif
   return cuda_status(mx::launch_gemm(tm_w, tm_a, args, plan, pdl, stream));
 }
 
@@ -159,6 +174,10 @@ int mx_create(mx_handle** out, int device) {
       if (mx::set_gemm_attributes() != cudaSuccess || mx::set_wo_a_attributes() != cudaSuccess ||
           cudaMalloc(&h->d_status, 16) != cudaSuccess ||
           cudaMemset(h->d_status, 0, 16) != cudaSuccess ||
+#ifdef MX_TIMELINE
+          cudaMalloc(&h->d_tl, kTimelineBytes) != cudaSuccess ||
+          cudaMemset(h->d_tl, 0, kTimelineBytes) != cudaSuccess ||
+#endif
           cudaDeviceSynchronize() != cudaSuccess)
         rc = MX_ERR_CUDA;
     }
@@ -179,6 +198,9 @@ int mx_destroy(mx_handle* h) {
   cudaGetDevice(&prev);
   cudaSetDevice(h->device);
   cudaFree(h->d_status);
+#ifdef MX_TIMELINE
+  cudaFree(h->d_tl);
+#endif
   cudaSetDevice(prev);
   delete h;
   return MX_OK;
@@ -407,6 +429,27 @@ int mx_wait_selftest(mx_handle* h, void* stream) {
   if (rc != MX_OK) return rc;
   return cuda_status(mx::launch_wait_selftest(h->d_status, static_cast<cudaStream_t>(stream)));
 }
+
+#ifdef MX_TIMELINE
+// Timeline build only (not declared in mx.h): the stamps of the GEMM launches
+// made since the last reset, launch after launch, kTimelineCtas x
+// kTimelineSlots each. Copies min(bytes, recorded) to host memory and returns
+// the number of launches recorded; reset clears the record.
+int mx_timeline_read(mx_handle* h, void* host, size_t bytes, int* launches) {
+  if (h == nullptr || host == nullptr || launches == nullptr) return MX_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
+  const size_t per = sizeof(unsigned long long) * mx::kTimelineCtas * mx::kTimelineSlots;
+  const size_t n = std::min(bytes, per * static_cast<size_t>(h->tl_next));
+  if (cudaMemcpy(host, h->d_tl, n, cudaMemcpyDeviceToHost) != cudaSuccess) return MX_ERR_CUDA;
+  *launches = h->tl_next;
+  return MX_OK;
+}
+int mx_timeline_reset(mx_handle* h) {
+  if (h == nullptr) return MX_ERR_INVALID_ARG;
+  h->tl_next = 0;
+  return cudaMemset(h->d_tl, 0, kTimelineBytes) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+#endif
 
 const char* mx_status_string(int s) {
   switch (s) {

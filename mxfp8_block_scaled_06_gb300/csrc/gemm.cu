@@ -46,6 +46,28 @@ namespace mx {
 namespace {
 
 constexpr int kThreads = 128;
+
+// Timeline build (-DMX_TIMELINE): %globaltimer stamps of one CTA's phases,
+// written to p.tl[cta * kTimelineSlots + slot]: 0 entry, 1 set-up done, 2 first
+// weight box issued, 3 weight scale tiles landed, 4 grid-dependency wait
+// returned, 5 first chunk landed, 6 accumulator complete, 7 reduction barrier
+// passed, 8 reduction done, 9 exit, 10 SM id, 11 chunks in the K-range.
+#ifdef MX_TIMELINE
+#define MX_TL(slot, v)                                                             \
+  do {                                                                             \
+    if (p.tl != nullptr)                                                           \
+      p.tl[(blockIdx.y * gridDim.x + blockIdx.x) * kTimelineSlots + (slot)] = (v); \
+  } while (0)
+__device__ __forceinline__ unsigned long long tl_smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+#else
+#define MX_TL(slot, v) \
+  do {                 \
+  } while (0)
+#endif
 constexpr uint32_t kWTileBytes = 128 * 128;  // one weight box: 128 rows x 128 K-bytes
 constexpr uint32_t kSfTileBytes = 512;       // one 128x4 scale tile
 
@@ -106,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int a_k0 = p.group_tiles > 0 ? (tile / p.group_tiles) * p.K : 0;
   const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S, kFusedA, min(p.M, kRowBatch));
   const int nsfb = L.nsfb;
+  if (threadIdx.x == 0) MX_TL(0, globaltimer());
 
   const uint32_t bars = base + L.bars;
   // full(s): weight box and activation box of stage s landed (two arrivals);
@@ -140,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t sfa_col = tmem_sfa_col(p.mtile);
   const uint32_t sfb_col = sfa_col + 4 * stages;
+  if (threadIdx.x == 0) MX_TL(1, globaltimer());
 
   auto fail = [&]() {
     atomicOr(p.status, kStatusTimeout);
@@ -170,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- before the grid-dependency wait: weights only
   if (w_lane && lane < n) issue_w(lane, lane);
   if (warp == 0) issued_n = min(n, stages);
+  if (warp == 0 && lane == 0) MX_TL(2, globaltimer());
   if (warp == 2 && lane == 0) {
     mbar_expect_tx(sfa_bar, static_cast<uint32_t>(n) * kSfTileBytes);
     bulk_load(base + L.sfa_off(0),
@@ -177,7 +202,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               static_cast<uint32_t>(n) * kSfTileBytes, sfa_bar, pol_w);
   }
   pdl_launch_dependents();
+#ifdef MX_TIMELINE
+  // the MMA warp, which has nothing to do before the grid-dependency wait,
+  // watches the weight scale tiles land (a non-consuming wait); a lane of a warp
+  // whose other lanes sit in griddepcontrol.wait could not record before it returns
+  if (warp == 1 && mbar_wait(sfa_bar, 0) && lane == 0) MX_TL(3, globaltimer());
+  if (threadIdx.x == 0) MX_TL(10, tl_smid());
+  if (threadIdx.x == 0) MX_TL(11, static_cast<unsigned long long>(n));
+#endif
   pdl_wait();
+  if (threadIdx.x == 0) MX_TL(4, globaltimer());
 
   // ---------------- activations (written by the previous kernel on the stream)
   int x_batches = 0;  // bf16 row batches requested (fused), warp 3
@@ -340,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) fail();
           break;
         }
+        if (i == 0 && lane == 0) MX_TL(5, globaltimer());
         tc_fence_after();
         if (elect_one()) {
           tmem_cp_32x128b_x4_lh(ta, f_lo, sf_hi);
@@ -381,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------- epilogue: TMEM -> shared partials
   if (!mbar_wait(accum_bar, 0)) fail();
+  if (threadIdx.x == 0) MX_TL(6, globaltimer());
   tc_fence_after();
   __syncwarp();
   float* const red = reinterpret_cast<float*>(base_ptr);
@@ -395,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   cluster_sync();
+  if (threadIdx.x == 0) MX_TL(7, globaltimer());
 
   // ---------------- cluster reduction + bf16 (+ MXFP8) store
   if (ok) {
@@ -438,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (threadIdx.x == 0) MX_TL(8, globaltimer());
   // the peers' reads of this CTA's partials have completed (their values were
   // consumed), so ordering the exits needs no memory release
   cluster_sync_relaxed();
@@ -457,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
+  if (threadIdx.x == 0) MX_TL(9, globaltimer());
 }
 
 int pow2_at_least(int v) {

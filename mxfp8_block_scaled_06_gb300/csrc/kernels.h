@@ -64,7 +64,16 @@ struct GemmArgs {
   uint8_t* q_scales;  // swizzled scales of q
   int q_cols;
   int* status;
+#ifdef MX_TIMELINE
+  unsigned long long* tl;  // kTimelineSlots %globaltimer stamps per CTA, or null
+#endif
 };
+
+#ifdef MX_TIMELINE
+// Timeline build only: stamps per CTA of one GEMM launch (see gemm.cu).
+constexpr int kTimelineSlots = 12;
+constexpr int kTimelineCtas = 512;
+#endif
 
 GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a = false);
 cudaError_t set_gemm_attributes();

@@ -9,7 +9,8 @@
  *
  * Conventions shared by every entry point:
  *  - Every data pointer is a DEVICE pointer owned by the caller. No call
- *    allocates or frees memory; the handle owns only a 4-byte status word.
+ *    allocates or frees memory; the handle owns only a 4-byte status word
+ *    (mx_gemm_chain_noalloc also uses a fixed array inside the library).
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL is the legacy default stream) and must be made with the handle's
  *    device current.
@@ -172,6 +173,36 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
                        const mx_weight w[3], int g1_cols, const void* norm_weight, float eps,
                        void* out1, void* a2, void* a2_scales, void* a3, void* a3_scales,
                        void* out, void* debug_y, void* debug_out2, void* stream);
+
+/* mx_gemm_chain for callers that cannot allocate device memory. Some callers
+ * have no way to provide the chain's two intermediate buffers: code that runs
+ * while a stream is being captured into a CUDA graph (cudaMalloc is not a
+ * stream operation and may synchronize the device), engines that hand a
+ * kernel library only the input and output buffers because they budget every
+ * byte of device memory themselves, and plugin hosts with no allocator exposed
+ * to the plugin. This entry point takes only the inputs and the output:
+ *   out = G3(MXFP8(G2(MXFP8(G1(a1)[:, :g1_cols])))), exactly as mx_gemm_chain
+ * computes it with debug_out1 = debug_out2 = NULL.
+ * The intermediates (a2 and a3 with their swizzled scales, each rounded up to
+ * 256 bytes) live in one fixed 1 MiB device array inside the library, which
+ * every GPU that loads the library holds until the process exits. The call
+ * allocates nothing and calls no allocating routine.
+ * Limit: round256(M*g1_cols) + round256(mx_scale_bytes(M, g1_cols)) +
+ * round256(M*w[1].n) + round256(mx_scale_bytes(M, w[1].n)) <= 1 MiB (for
+ * g1_cols = 1536 and w[1].n = 8192: M <= 99); larger problems return
+ * MX_ERR_UNSUPPORTED before anything is launched - use mx_gemm_chain with
+ * caller buffers then.
+ * The first call on a device looks up the array's device address with that
+ * device current (a one-time set-up per device); make that first call before
+ * any stream capture. Every call shares the array, and it keeps the last call's
+ * contents: each byte the kernels read is written earlier in the same call, so
+ * nothing has to start at zero. Calls whose work overlaps on the GPU (two
+ * streams, or a graph replay next to another call) race on the array: order
+ * them on one stream. The paper has no counterpart: this is an addition for
+ * callers without an allocator.
+ * Other arguments, constraints and errors as in mx_gemm_chain. */
+int mx_gemm_chain_noalloc(mx_handle* h, int M, const void* a1, const void* a1_scales,
+                          const mx_weight w[3], int g1_cols, void* out, void* stream);
 
 /* Grouped WO-A with RoPE, writing MXFP8 for wo_b (`dsv41_o_proj` and
  * `_can_fuse_wo_a` on the page "vllm.models.deepseek_v41.nvidia.ops.o_proj").

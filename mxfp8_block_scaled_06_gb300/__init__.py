@@ -24,7 +24,7 @@ MX_FLAG_PDL = 1
 
 EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows",
            "mx_rmsnorm_quantize_rows", "mx_gemm", "mx_gemm_bf16", "mx_gemm_chain",
-           "mx_gemm_chain_norm", "wo_a_grouped", "wo_a_grouped_unfused", "mx_device_status",
+           "mx_gemm_chain_norm", "mx_gemm_chain_noalloc", "wo_a_grouped", "wo_a_grouped_unfused", "mx_device_status",
            "mx_wait_selftest", "mx_status_string"]
 
 _vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx_gemm_bf16.argtypes = [_vp, _i, _i, _i, _vp, _l, _vp, _vp, _vp, _u, _vp]
     lib.mx_gemm_chain.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp]
+    lib.mx_gemm_chain_noalloc.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp]
     lib.wo_a_grouped.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i,
                                  _vp, _vp, _vp, _vp, _vp, _i, _vp]
     lib.wo_a_grouped_unfused.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i,
@@ -311,6 +312,31 @@ def mx_gemm_chain(h: Handle, a1, a1_scales, weights, g1_cols: int = 1536, out=No
                                         _ptr(a2_scales), _ptr(a3), _ptr(a3_scales), _ptr(out),
                                         _ptr(d1), _ptr(d2), _stream(stream)), "mx_gemm_chain")
     return dict(out=out, a2=a2, a2_scales=a2_scales, a3=a3, a3_scales=a3_scales, out1=d1, out2=d2)
+
+
+def mx_gemm_chain_noalloc(h: Handle, a1, a1_scales, weights, g1_cols: int = 1536, out=None,
+                          stream=None):
+    """The chain for callers that cannot allocate device memory: only the inputs
+    and the output are passed; the library keeps the two intermediates in a fixed
+    1 MiB device array (see include/mx.h). Raises MxError (MX_ERR_UNSUPPORTED)
+    when the intermediates do not fit; calls that overlap on the GPU race."""
+    import torch
+    if len(weights) != 3:
+        raise ValueError("weights: three (w, w_scales) pairs are required")
+    (_, k1), _, (n3, _) = (_weight(i, w, s) for i, (w, s) in enumerate(weights))
+    m = a1.shape[0]
+    _matrix("a1", a1, _codes_types(), m, k1)
+    _flat("a1_scales", a1_scales, _scale_types(), _sbytes(m, k1))
+    out = torch.empty((m, n3), dtype=torch.bfloat16, device=a1.device) if out is None else out
+    _matrix("out", out, (torch.bfloat16,), m, n3)
+    ws = (MxWeight * 3)(*[MxWeight(_ptr(w), _ptr(s), w.shape[0], w.shape[1]) for w, s in weights])
+    _resident(h, a1=a1, a1_scales=a1_scales, out=out,
+              **{f"weight {i}": w for i, (w, _) in enumerate(weights)},
+              **{f"weight {i} scales": s for i, (_, s) in enumerate(weights)})
+    _check(load_library().mx_gemm_chain_noalloc(h.ptr, m, _ptr(a1), _ptr(a1_scales), ws, g1_cols,
+                                                _ptr(out), _stream(stream)),
+           "mx_gemm_chain_noalloc (the intermediates must fit in the library's 1 MiB array)")
+    return out
 
 
 def mx_rmsnorm_quantize_rows(h: Handle, x, norm_weight, eps: float, q=None, scales=None,

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
+#include <mutex>
 #include <new>
 
 #include "../../include/mx.h"
@@ -409,6 +410,58 @@ int wo_a_grouped_unfused(mx_handle* h, int T, const void* x, long ldx, const int
   //    to bf16 and requantized in the epilogue
   return gemm_launch(h, T, G * R, H * D, xq, xq_scales, w, w_scales, z, static_cast<uint8_t*>(q),
                      static_cast<uint8_t*>(q_scales), G * R, true, s, nullptr, 0, G);
+}
+
+// ------------------------------------------------ chain without allocation
+// mx_gemm_chain_noalloc keeps the chain's two MXFP8 intermediates (codes and
+// swizzled scales of the second and third projections' inputs) in this fixed
+// device array instead of caller buffers. Every GPU that loads the library
+// holds it until the process exits. Host code may not use the array's name as
+// a device address (on the host it names a stand-in): the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+constexpr size_t kChainScratchBytes = size_t{1} << 20;
+static __device__ __align__(256) uint8_t g_chain_scratch[kChainScratchBytes];
+
+namespace {
+
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_address[kScratchDevices] = {};
+
+// Device address of g_chain_scratch on `device` (the current device), looked up
+// on the first call for that device.
+int chain_scratch(int device, uint8_t** out) {
+  if (device < 0 || device >= kScratchDevices) return MX_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_address[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_chain_scratch) != cudaSuccess || p == nullptr) return MX_ERR_CUDA;
+    g_scratch_address[device] = p;
+  }
+  *out = static_cast<uint8_t*>(g_scratch_address[device]);
+  return MX_OK;
+}
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+int mx_gemm_chain_noalloc(mx_handle* h, int M, const void* a1, const void* a1_scales,
+                          const mx_weight w[3], int g1_cols, void* out, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  if (w == nullptr || M < 1 || g1_cols < 1 || w[1].n < 1) return MX_ERR_INVALID_ARG;
+  // a2 [M, g1_cols] + its scales, a3 [M, w[1].n] + its scales, each 256-byte aligned
+  const size_t a2 = round256(static_cast<size_t>(M) * static_cast<size_t>(g1_cols));
+  const size_t s2 = round256(mx_scale_bytes(M, g1_cols));
+  const size_t a3 = round256(static_cast<size_t>(M) * static_cast<size_t>(w[1].n));
+  const size_t s3 = round256(mx_scale_bytes(M, w[1].n));
+  if (a2 + s2 + a3 + s3 > kChainScratchBytes) return MX_ERR_UNSUPPORTED;
+  uint8_t* p = nullptr;
+  rc = chain_scratch(h->device, &p);
+  if (rc != MX_OK) return rc;
+  return mx_gemm_chain(h, M, a1, a1_scales, w, g1_cols, p, p + a2, p + a2 + s2, p + a2 + s2 + a3,
+                       out, nullptr, nullptr, stream);
 }
 
 int mx_device_status(mx_handle* h, int* status) {

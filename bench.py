@@ -40,7 +40,7 @@ CHAIN_SHAPES = [(2048, 5120), (8192, 1536), (5120, 8192)]
 CHAIN_G1_COLS = 1536
 CHAIN_M = (1, 4, 8, 16, 32, 48, 64)
 WOA = dict(G=4, H=8, R=1024, D=512)
-WOA_T = (1, 8, 32)
+WOA_T = (1, 8, 16, 32)
 WOB = (5120, 4096)
 SWEEP_M = (64, 96, 128, 192, 256)
 SWEEP_SHAPES = [(8192, 5120), (5120, 8192)]
@@ -120,9 +120,13 @@ class Rig:
         return self.torch.from_numpy(bits.view(np.int16)).view(self.torch.bfloat16).to(self.dev)
 
 
+REPLAYS = 10  # every timing is the median of at least this many graph replays
+
+
 def time_graph(torch, fn, reps, per_graph, stream):
-    """Capture per_graph calls of fn into a CUDA graph, replay it reps times;
-    returns total device milliseconds (CUDA events on the capturing stream)."""
+    """Capture per_graph calls of fn into a CUDA graph and replay it reps times,
+    each replay bracketed by CUDA events on the capturing stream; returns the
+    per-replay device milliseconds and the graph."""
     with torch.cuda.stream(stream):
         fn(0)  # make sure everything is initialized outside capture
         torch.cuda.synchronize()
@@ -131,16 +135,28 @@ def time_graph(torch, fn, reps, per_graph, stream):
             for i in range(per_graph):
                 fn(i)
     torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     with torch.cuda.stream(stream):  # replay() launches on the current stream
         g.replay()
         torch.cuda.synchronize()
-        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(reps):
+        for st, sp in ev:
+            st.record(stream)
             g.replay()
-        stop.record(stream)
-    stop.synchronize()
-    return start.elapsed_time(stop), g
+            sp.record(stream)
+    ev[-1][1].synchronize()
+    return [st.elapsed_time(sp) for st, sp in ev], g
+
+
+def median_us(torch, fn, per_graph, stream, reps=REPLAYS):
+    """Median over reps replays of a per_graph-call graph, in us per call."""
+    times, _ = time_graph(torch, fn, reps, per_graph, stream)
+    return statistics.median(times) * 1e3 / per_graph
+
+
+def step_replays(k):
+    """Replays of a fixed-size graph that time exactly k steps: the smallest
+    divisor of k that is at least min(10, k)."""
+    return next(d for d in range(min(REPLAYS, k), k + 1) if k % d == 0)
 
 
 class Clocks:
@@ -248,8 +264,10 @@ def run_ours(args):
                 mx.mx_quantize_rows(h, xs[m], q=qa[m][0], scales=qa[m][1], stream=stream)
             mx.mx_gemm(h, qa[m][0], qa[m][1], wq, ws, out=outs[m], pdl=True, stream=stream)
 
-    per_graph = min(K, 100)
-    reps = max(1, K // per_graph)
+    # exactly K steps timed: `reps` replays of a graph of K / reps steps, each
+    # replay bracketed by events; ms per step = the median replay / its steps
+    reps = step_replays(K)
+    per_graph = K // reps
     k_eff = reps * per_graph
     # warm-up: W steps untimed, then a sustained window so the clock sampler sees load
     for i in range(max(W, 3)):
@@ -258,24 +276,26 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks = Clocks(local)
     t_end = time.time() + 1.0
-    ms_total, g_step = time_graph(torch, step, reps, per_graph, stream)
+    _, g_step = time_graph(torch, step, 1, per_graph, stream)
     with torch.cuda.stream(stream):
         while time.time() < t_end:
             g_step.replay()
     torch.cuda.synchronize()
     rep.barrier()
     torch.cuda.synchronize()
-    st, sp = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     with torch.cuda.stream(stream):
-        st.record(stream)
-        for _ in range(reps):
+        for st, sp in ev:
+            st.record(stream)
             g_step.replay()
-        sp.record(stream)
-    sp.synchronize()
-    ms_total = st.elapsed_time(sp)
+            sp.record(stream)
+    ev[-1][1].synchronize()
+    torch.cuda.synchronize()
+    rep.barrier()
     clk = clocks.stop()
-    ms_total = rep.max_over_ranks(ms_total)
-    ms_step = ms_total / k_eff
+    replay_ms = [st.elapsed_time(sp) for st, sp in ev]
+    ms_step = rep.max_over_ranks(statistics.median(replay_ms) / per_graph)
+    st, sp = ev[0]
     value = rep.job_value(step_bytes(), ms_step)
 
     # ------------------------------------------------- per-kernel GEMM timing
@@ -284,9 +304,7 @@ def run_ours(args):
         def only(i, m=m):
             wq, ws = wts[i % nset][0]
             mx.mx_gemm(h, qa[m][0], qa[m][1], wq, ws, out=outs[m], pdl=True, stream=stream)
-        n_launch = 400
-        ms, _ = time_graph(torch, only, 5, n_launch, stream)
-        us = ms * 1e3 / (5 * n_launch)
+        us = median_us(torch, only, 100, stream)
         gemm_us[m] = us
         gemm_gbs[m] = gemm_bytes(m, N1, K1) / (us * 1e-6) / 1e9
     # the same step with the quantization inside the GEMM (mx_gemm_bf16: one
@@ -296,18 +314,15 @@ def run_ours(args):
         def fused(i, m=m):
             wq, ws = wts[i % nset][0]
             mx.mx_gemm_bf16(h, xs[m], wq, ws, out=outs[m], pdl=True, stream=stream)
-        ms, _ = time_graph(torch, fused, 5, 400, stream)
-        fused_us[m] = ms * 1e3 / (5 * 400)
+        fused_us[m] = median_us(torch, fused, 100, stream)
     # dominant kernel: mx_gemm over the step's mix of M
-    ms, _ = time_graph(torch, lambda i: step(i, quant=False), 5, 100, stream)
-    gemm_launch_us = ms * 1e3 / (5 * 100 * len(M_LIST))
+    gemm_launch_us = median_us(torch, lambda i: step(i, quant=False), 100, stream) / len(M_LIST)
     gemm_mix_bytes = sum(gemm_bytes(m, N1, K1) for m in M_LIST) / len(M_LIST)
     achieved = gemm_mix_bytes / (gemm_launch_us * 1e-6) / 1e9
     quant_us = {}
     for m in (1, 8):
-        ms, _ = time_graph(torch, lambda i, m=m: mx.mx_quantize_rows(
-            h, xs[m], q=qa[m][0], scales=qa[m][1], stream=stream), 5, 200, stream)
-        quant_us[m] = ms * 1e3 / 1000
+        quant_us[m] = median_us(torch, lambda i, m=m: mx.mx_quantize_rows(
+            h, xs[m], q=qa[m][0], scales=qa[m][1], stream=stream), 100, stream)
 
     # ----------------------------------------------------------------- chain
     chain = {}
@@ -326,8 +341,7 @@ def run_ours(args):
 
             def run_chain(i, m=m, q1=q1, bufs=bufs):
                 mx.mx_gemm_chain(h, q1[0], q1[1], cw[i % cset], g1_cols=CHAIN_G1_COLS, stream=stream, **bufs)
-            ms, _ = time_graph(torch, run_chain, 5, 60, stream)
-            us = ms * 1e3 / 300
+            us = median_us(torch, run_chain, 30, stream)
             chain[m] = {"us": round(us, 3), "weight_gbs": round(wbytes / (us * 1e-6) / 1e9, 1),
                         "vs_weight_read_at_peak": round(us / (wbytes / (pk["hbm_gbs"] * 1e9) * 1e6), 3)}
             # the same chain with the RMS-norm split between G1 and G2 (one more launch)
@@ -338,8 +352,7 @@ def run_ours(args):
             def run_norm(i, m=m, q1=q1, bufs=bufs, out1=out1, nw=nw):
                 mx.mx_gemm_chain_norm(h, q1[0], q1[1], cw[i % cset], nw, 1e-6, g1_cols=CHAIN_G1_COLS,
                                       out1=out1, stream=stream, **bufs)
-            ms, _ = time_graph(torch, run_norm, 5, 60, stream)
-            chain[m]["with_rms_norm_split_us"] = round(ms * 1e3 / 300, 3)
+            chain[m]["with_rms_norm_split_us"] = round(median_us(torch, run_norm, 30, stream), 3)
 
     # ------------------------------------------------------- WO-A and wo_b
     woa = {}
@@ -373,32 +386,34 @@ def run_ours(args):
                 wq, ws = ww[i % wset][0]
                 mx.wo_a_grouped_unfused(h, x, pos, cs, wq, ws, G, H, R, q=q, q_scales=qs, xq=xq,
                                         xq_scales=xqs, stream=stream)
-            ms_a, _ = time_graph(torch, run_woa, 5, 60, stream)
-            ms_p, _ = time_graph(torch, run_pair, 5, 60, stream)
-            ms_u, _ = time_graph(torch, run_unfused, 5, 60, stream)
-            ua, up, uu = ms_a * 1e3 / 300, ms_p * 1e3 / 300, ms_u * 1e3 / 300
+            ua = median_us(torch, run_woa, 30, stream)
+            up = median_us(torch, run_pair, 30, stream)
+            uu = median_us(torch, run_unfused, 30, stream)
             wa = w_bytes(*pair[0])
             woa[t] = {"wo_a_us": round(ua, 3), "wo_a_weight_gbs": round(wa / (ua * 1e-6) / 1e9, 1),
                       "wo_a_plus_wo_b_us": round(up, 3),
                       "pair_weight_gbs": round((wa + w_bytes(*WOB)) / (up * 1e-6) / 1e9, 1),
-                      "wo_a_unfused_us": round(uu, 3)}
+                      "wo_a_unfused_us": round(uu, 3),
+                      "wo_a_path": "fused kernel" if t <= 8 else "two launches on the handle's scratch"}
 
     # --------------------------------------------------------------- sweep
     sweep = {}
-    if args.sweep:
+    mxfp8_peak = 2 * pk["bf16_tflops"]  # the nominal fp8 : bf16 dense ratio times the measured bf16 burst
+    if not args.quick:
         for n, k in SWEEP_SHAPES:
             sset = rig.copies(w_bytes(n, k))
             sw = rig.weight_set([(n, k)], seed=4, ncopies=sset)
             for m in SWEEP_M:
                 a = mx.mx_quantize_rows(h, rig.activation(m, k, seed=4))
                 o = torch.empty((m, n), dtype=torch.bfloat16, device=rig.dev)
-                ms, _ = time_graph(torch, lambda i, a=a, o=o: mx.mx_gemm(
-                    h, a[0], a[1], *sw[i % sset][0], out=o, pdl=True, stream=stream), 5, 100, stream)
-                us = ms * 1e3 / 500
+                us = median_us(torch, lambda i, a=a, o=o: mx.mx_gemm(
+                    h, a[0], a[1], *sw[i % sset][0], out=o, pdl=True, stream=stream), 50, stream)
                 tf = 2 * m * n * k / (us * 1e-6) / 1e12
-                sweep[f"M{m}_N{n}_K{k}"] = {"us": round(us, 3),
-                                            "gbs": round(gemm_bytes(m, n, k) / (us * 1e-6) / 1e9, 1),
-                                            "tflops": round(tf, 1)}
+                gbs = gemm_bytes(m, n, k) / (us * 1e-6) / 1e9
+                sweep[f"M{m}_N{n}_K{k}"] = {"us": round(us, 3), "gbs": round(gbs, 1),
+                                            "hbm_frac": round(gbs / pk["hbm_gbs"], 3),
+                                            "tflops": round(tf, 1),
+                                            "tensor_frac": round(tf / mxfp8_peak, 3)}
 
     # --------------------------------------------------- end to end (host I/O)
     # the step's four activations travel as one pinned host buffer and its four
@@ -434,8 +449,7 @@ def run_ours(args):
     e_ms_eager = st.elapsed_time(sp) / e_steps
     # as a decode server runs it: the same calls, copies included, captured once in
     # a CUDA graph (per_graph steps) and replayed
-    ms_g, _ = time_graph(torch, e2e_step, reps, per_graph, stream)
-    e_ms = ms_g / k_eff
+    e_ms = median_us(torch, e2e_step, per_graph, stream, reps) / 1e3
     e2e = {"value": round(world * step_bytes() / (e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "path": "public API (mx_quantize_rows, mx_gemm) through the Python binding, with one "
@@ -469,13 +483,17 @@ def run_ours(args):
                    "step_bytes": step_bytes(), "pdl": True, "parallelism": f"replicas x{world}",
                    "l2": f"weights rotate over {nset} copies ({nset * w_bytes(N1, K1) / 1e6:.0f} MB "
                          f">= 3x L2 {l2 / 1e6:.0f} MB): inputs larger than L2",
-                   "timing": f"CUDA graph of {per_graph} steps replayed {reps}x, CUDA events"},
+                   "timing": f"median of {reps} replays of a CUDA graph of {per_graph} steps (CUDA "
+                             f"events per replay); per-kernel, chain, WO-A and sweep figures: median "
+                             f"of {REPLAYS} replays"},
         "gemm_us": {str(m): round(v, 3) for m, v in gemm_us.items()},
         "gemm_gbs": {str(m): round(v, 1) for m, v in gemm_gbs.items()},
         "gemm_frac_of_peak": {str(m): round(v / pk["hbm_gbs"], 3) for m, v in gemm_gbs.items()},
         "quantize_us": {str(m): round(v, 3) for m, v in quant_us.items()},
         "quantize_plus_gemm_fused_us": {str(m): round(v, 3) for m, v in fused_us.items()},
         "chain_us_per_step": chain, "wo_a": woa, "sweep": sweep,
+        "sweep_peaks": {"hbm_gbs": pk["hbm_gbs"], "mxfp8_tflops": mxfp8_peak,
+                        "mxfp8_peak_kind": f"2 x {pk_kind} bf16 burst"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": k_eff * 2 * len(M_LIST), "clocks": clk, "device_status": status,
     }
@@ -606,8 +624,10 @@ def run_profile(args):
     print(json.dumps({"profile": args.profile, "ok": True}))
 
 
-TIMELINE_SLOTS = ("entry", "setup", "w_issued", "wsf_landed", "wait_ret", "first_full", "accum",
-                  "red_pass", "red_done", "exit")
+TIMELINE_SLOTS = {"entry": 0, "setup": 1, "w_issued": 2, "wsf_landed": 3, "wait_ret": 4,
+                  "rms_done": 13, "x_landed": 14, "act_quantized": 12, "first_full": 5, "accum": 6, "red_pass": 7, "red_done": 8,
+                  "exit": 9}
+TIMELINE_EXIT = TIMELINE_SLOTS["exit"]
 
 
 def run_timeline(args):
@@ -627,14 +647,16 @@ def run_timeline(args):
     lib.mx_timeline_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                      ctypes.POINTER(ctypes.c_int)]
     lib.mx_timeline_reset.argtypes = [ctypes.c_void_p]
-    ctas, slots, launches = 512, 12, 256
+    ctas, slots, launches = 512, 16, 256
     torch.cuda.set_device(0)
     h = mx.mx_create(0)
     props = torch.cuda.get_device_properties(0)
     rig = Rig(torch, mx, h, getattr(props, "L2_cache_size", 126 * 2**20))
     stream = torch.cuda.Stream()
 
-    def record(fn, per_graph):
+    def record(fn, per_graph, period=1, names=None):
+        """Timeline of per_graph calls of fn. period > 1: each call makes
+        `period` launches, reported separately (by `names`)."""
         with torch.cuda.stream(stream):
             fn(0)  # tensor maps and plans outside the capture
         torch.cuda.synchronize()
@@ -658,37 +680,51 @@ def run_timeline(args):
         buf = np.zeros(launches * ctas * slots, dtype=np.uint64)
         assert lib.mx_timeline_read(h.ptr, buf.ctypes.data, buf.nbytes, ctypes.byref(n)) == 0
         tl = buf.reshape(launches, ctas, slots)[: n.value]
-        phases = {k: [] for k in TIMELINE_SLOTS}
-        dur, early, landed_early = [], [], []
-        for i in range(1, len(tl)):
-            prev = tl[i - 1][tl[i - 1][:, 9] > 0]
-            cur = tl[i][tl[i][:, 9] > 0]
-            if len(prev) == 0 or len(cur) == 0:
-                continue
-            p_end = int(prev[:, 9].max())
-            rel = cur[:, :10].astype(np.int64) - p_end
-            dur.append((int(cur[:, 9].max()) - p_end) / 1e3)
-            early.append(float((rel[:, 0] < 0).mean()))
-            landed_early.append(float(((rel[:, 3] < 0) & (cur[:, 3] > 0)).mean()))
-            for j, k in enumerate(TIMELINE_SLOTS):
-                v = rel[:, j][cur[:, j] > 0]
-                if len(v):
-                    phases[k].append(float(np.median(v)))
-        return {"us_per_graph_item": round(ms * 1e3 / (5 * per_graph), 3),
+        e = TIMELINE_EXIT
+        res = {}
+        for pos in range(period):
+            phases = {k: [] for k in TIMELINE_SLOTS}
+            spread = {k: [] for k in TIMELINE_SLOTS}
+            dur, early, landed_early = [], [], []
+            for i in range(pos if pos > 0 else period, len(tl), period):
+                prev = tl[i - 1][tl[i - 1][:, e] > 0]
+                cur = tl[i][tl[i][:, e] > 0]
+                if len(prev) == 0 or len(cur) == 0:
+                    continue
+                p_end = int(prev[:, e].max())
+                rel = cur.astype(np.int64) - p_end
+                dur.append((int(cur[:, e].max()) - p_end) / 1e3)
+                early.append(float((rel[:, 0] < 0).mean()))
+                landed_early.append(float(((rel[:, 3] < 0) & (cur[:, 3] > 0)).mean()))
+                for k, j in TIMELINE_SLOTS.items():
+                    v = rel[:, j][cur[:, j] > 0]
+                    if len(v):
+                        phases[k].append(float(np.median(v)))
+                        spread[k].append(float(v.max() - v.min()))
+            res[names[pos] if names else pos] = {
                 "launch_us_median": round(float(np.median(dur)), 3) if dur else None,
                 "ctas_started_before_previous_end": round(float(np.median(early)), 3) if early else None,
                 "weight_scales_landed_before_previous_end": round(float(np.median(landed_early)), 3)
                 if landed_early else None,
-                "phase_ns_vs_previous_end": {k: int(np.median(v)) for k, v in phases.items() if v}}
+                "phase_ns_vs_previous_end": {k: int(np.median(v)) for k, v in phases.items() if v},
+                "phase_spread_ns_over_ctas": {k: int(np.median(v)) for k, v in spread.items() if v}}
+        out = {"us_per_graph_item": round(ms * 1e3 / (5 * per_graph), 3)}
+        if period == 1:
+            out.update(res[0])
+        else:
+            out["launches"] = res
+        return out
 
     out = {}
     nset = rig.copies(w_bytes(N1, K1))
     wts = rig.weight_set([(N1, K1)], seed=1, ncopies=nset)
-    for m in (1, 8):
+    for m in (1, 8, 64):
         q = mx.mx_quantize_rows(h, rig.activation(m, K1, seed=1))
         o = torch.empty((m, N1), dtype=torch.bfloat16, device=rig.dev)
-        out[f"gemm_M{m}"] = record(lambda i, q=q, o=o: mx.mx_gemm(
-            h, q[0], q[1], *wts[i % nset][0], out=o, pdl=True, stream=stream), 12)
+        for pdl in (True, False):
+            out[f"gemm_M{m}" + ("" if pdl else "_no_pdl")] = record(
+                lambda i, q=q, o=o, pdl=pdl: mx.mx_gemm(h, q[0], q[1], *wts[i % nset][0], out=o, pdl=pdl,
+                                                        stream=stream), 12)
     xs = {m: rig.activation(m, K1, seed=1) for m in M_LIST}
     qa = {m: mx.mx_quantize_rows(h, xs[m]) for m in M_LIST}
     outs = {m: torch.empty((m, N1), dtype=torch.bfloat16, device=rig.dev) for m in M_LIST}
@@ -710,10 +746,45 @@ def run_timeline(args):
                     a3_scales=torch.empty(mx.mx_scale_bytes(m, CHAIN_SHAPES[1][0]), dtype=torch.uint8,
                                           device=rig.dev))
         out[f"chain_M{m}"] = record(lambda i, q1=q1, bufs=bufs: mx.mx_gemm_chain(
-            h, q1[0], q1[1], cw[i % cset], g1_cols=CHAIN_G1_COLS, stream=stream, **bufs), 4)
+            h, q1[0], q1[1], cw[i % cset], g1_cols=CHAIN_G1_COLS, stream=stream, **bufs), 4,
+            period=3, names=("G1", "G2", "G3"))
+        out1 = torch.empty((m, CHAIN_SHAPES[0][0]), dtype=torch.bfloat16, device=rig.dev)
+        nw = torch.from_numpy(synth.norm_weight_bf16(4, CHAIN_G1_COLS).view(np.int16)).view(
+            torch.bfloat16).to(rig.dev)
+        out[f"chain_norm_M{m}"] = record(lambda i, q1=q1, bufs=bufs, out1=out1, nw=nw: mx.mx_gemm_chain_norm(
+            h, q1[0], q1[1], cw[i % cset], nw, 1e-6, g1_cols=CHAIN_G1_COLS, out1=out1, stream=stream,
+            **bufs), 4, period=3,
+            names=("G1", "G2+norm", "G3") if m <= 16 else ("G1", "G2 (after the norm kernel)", "G3"))
     torch.cuda.synchronize()
     assert mx.mx_device_status(h) == mx.MX_OK
     print(json.dumps({"timeline": out}))
+
+
+def launch_replicas(n):
+    """bench.py --gpus N outside torchrun: N processes of this script, rank i on
+    GPU i (RANK = LOCAL_RANK = i, WORLD_SIZE = N, rendezvous on 127.0.0.1), with
+    the same arguments; rank 0 alone prints. Returns the largest exit code."""
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    procs = []
+    for i in range(n):
+        env = dict(os.environ, RANK=str(i), LOCAL_RANK=str(i), WORLD_SIZE=str(n),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + sys.argv[1:], env=env))
+    return max(p.wait() for p in procs)
+
+
+def replica_selftest():
+    """--replica-selftest: the replicas' host-side coordination without a GPU (a
+    gloo barrier and the maximum over ranks of rank + 1); rank 0 prints it."""
+    rep = Replicas()
+    rep.barrier()
+    top = rep.max_over_ranks(float(rep.rank + 1))
+    if rep.reports:
+        print(json.dumps({"n_gpus": rep.world, "max_over_ranks": top}))
 
 
 def main():
@@ -723,7 +794,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the chain and WO-A extras")
-    ap.add_argument("--sweep", action="store_true", help="also time the M=64..256 row sweep")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
@@ -731,7 +801,14 @@ def main():
     ap.add_argument("--profile", default=None, choices=["gemm", "chain", "wo_a", "sweep"])
     ap.add_argument("--timeline", action="store_true",
                     help="per-CTA phase timeline of GEMM launches (builds the -DMX_TIMELINE library)")
+    ap.add_argument("--replica-selftest", action="store_true",
+                    help="the replicas' host-side coordination only (no GPU), e.g. with --gpus 2")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus))
+    if args.replica_selftest:
+        replica_selftest()
+        return
     if args.timeline:
         run_timeline(args)
         return

@@ -9,8 +9,12 @@
  *
  * Conventions shared by every entry point:
  *  - Every data pointer is a DEVICE pointer owned by the caller. No call
- *    allocates or frees memory; the handle owns only a 4-byte status word
- *    (mx_gemm_chain_noalloc also uses a fixed array inside the library).
+ *    allocates or frees memory. mx_create allocates the handle's device memory
+ *    once: a status word, the per-tile counters of the persistent chain kernel
+ *    (64 KiB), the activation scratch of wo_a_grouped's two-launch form
+ *    (8.25 MiB) and the block sums of squares of mx_gemm_chain_norm's
+ *    three-launch form (64 KiB); mx_gemm_chain_noalloc also uses a fixed
+ *    array inside the library.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL is the legacy default stream) and must be made with the handle's
  *    device current.
@@ -18,6 +22,10 @@
  *    outputs are left untouched and nothing is enqueued (the page
  *    "vllm.models.deepseek_v41.nvidia.ops.cute_dsl", `_consumer`: a bad
  *    argument raises before the call's first launch).
+ *  - MX_OK from a launching entry point means the work was enqueued. A bounded
+ *    device-side wait that expires makes the kernel skip its remaining work
+ *    instead of hanging, so the outputs of every call since the last check are
+ *    defined only once mx_device_status reports MX_OK.
  *  - Activation scales and weight scales use the F8_128x4 swizzled layout:
  *    the [rows, K/32] scale matrix is padded to ceil128(rows) x ceil4(K/32)
  *    and cut into 128x4 tiles of 512 contiguous bytes (tiles row-major); inside
@@ -67,7 +75,8 @@ typedef struct mx_weight {
 
 /* Create a handle for `device`. Checks compute capability 10.3 (the device
  * gate of `_cute_dsl_runner` / `_wide_supported` on the mxfp8 page), loads the
- * kernels and allocates the 4-byte device status word. The handle also caches
+ * kernels and allocates the handle's device memory (the status word, the
+ * persistent chain's counters, zeroed, and wo_a_grouped's scratch). The handle also caches
  * the tensor maps of the buffers it has seen (host memory only), so one handle
  * is used by one host thread at a time; give each thread its own handle.
  * Returns MX_ERR_DEVICE on another architecture, MX_ERR_CUDA if no device. */
@@ -95,7 +104,11 @@ int mx_quantize_rows(mx_handle* h, int M, int K, const void* x, long ldx,
 
 /* RMS normalization then MX quantization of each row: y = bf16(x / sqrt(mean
  * over the row of x^2 + eps) * norm_weight), computed in float32, then y
- * quantized as mx_quantize_rows does. This is the split between the first two
+ * quantized as mx_quantize_rows does. The squares are summed in a fixed order:
+ * per 32-block the pairwise tree over its elements (element j with j ^ 16, then
+ * j ^ 8, j ^ 4, j ^ 2, j ^ 1), then the block sums from the first block on;
+ * the reciprocal RMS is 1 / sqrt(sum / K + eps) with correctly rounded division
+ * and square root. This is the split between the first two
  * projections of a decode step (`qr, qr_scale, kv = attn._split_qkv_and_norm(
  * qr_kv)` in `AttentionStep.run`, step page; the pages show only the call: the
  * reading is an RMS norm of qr with a given weight and epsilon).
@@ -162,9 +175,18 @@ int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales,
 /* mx_gemm_chain with the split between G1 and G2 of `AttentionStep.run`:
  * G1 writes its whole bf16 output to out1 ([M, N1]: qr = columns [0, g1_cols),
  * kv = the rest, which the caller reads from out1), qr is RMS-normalized with
- * norm_weight / eps and MX-quantized into a2 / a2_scales
- * (mx_rmsnorm_quantize_rows), then G2 (+ requantization into a3) and G3 as in
- * mx_gemm_chain. Four launches on one stream, with PDL.
+ * norm_weight / eps and MX-quantized into a2 / a2_scales (bit for bit what
+ * mx_rmsnorm_quantize_rows writes), then G2 (+ requantization into a3) and G3
+ * as in mx_gemm_chain. On one stream, with PDL. Up to 16 rows in three
+ * launches: G1's epilogue also writes each 32-block's sum of squares of qr to
+ * the handle's scratch, and G2 reads qr in bf16, adds those sums in block
+ * order for each row's RMS and normalizes and quantizes the K-range it
+ * contracts in its prologue (the CTAs of the first weight tile also store a2,
+ * a2_scales and debug_y). Above 16 rows, where every CTA of G2 repeating the
+ * quantization of its K-range costs more than a launch, the norm kernel runs
+ * between G1 and G2 (four launches). Both forms give the same bits as
+ * mx_rmsnorm_quantize_rows between mx_gemm calls. Calls on one handle whose
+ * work overlaps on the GPU race on the scratch (as for wo_a_grouped).
  *   norm_weight [g1_cols] bf16, 16-byte aligned; eps >= 0.
  *   out1        [M, N1] bf16, required.
  *   debug_y     optional [M, g1_cols] bf16: the normalized qr before quantization.
@@ -226,7 +248,15 @@ int mx_gemm_chain_noalloc(mx_handle* h, int M, const void* a1, const void* a1_sc
  * Constraints: d_nope == 448, d_rope == 64, H <= 8, R % 128 == 0,
  * 1 <= T <= 128; else MX_ERR_UNSUPPORTED (the unfused path's domain).
  * early_trigger != 0: the dependent kernel (wo_b) may launch right after
- * this kernel has allocated its tensor memory (`dsv41_o_proj`). */
+ * this kernel has allocated its tensor memory (`dsv41_o_proj`).
+ * Above 8 tokens, when debug_xq and debug_xs are null and the quantized
+ * activation (T*G*H*D bytes plus its scales) fits the handle's 8.25 MiB
+ * scratch, the call runs wo_a_grouped_unfused's two launches on that scratch
+ * instead of the fused kernel (faster there on GB300: T = 32 takes 9.9 us
+ * against 15.8 us); q, q_scales and debug_z mean the same, the dependent kernel
+ * may launch once the second launch's GEMM releases it, and two such calls on
+ * one handle whose work overlaps on the GPU race on the scratch: give each
+ * stream its own handle. */
 int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* positions,
                  const float* cos_sin, int max_pos, const void* w, const void* w_scales,
                  int G, int H, int d_nope, int d_rope, int R, void* q, void* q_scales,
@@ -244,8 +274,9 @@ int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* po
  *   z          optional [T, G*R] bf16 (the pre-quantization output), or null.
  *   other arguments as in wo_a_grouped (H is not limited to 8 here).
  * q / q_scales equal mx_quantize_rows of bf16(z). On GB300 the fused kernel is
- * faster up to about 16 tokens and this path from 32 on (T = 32: 10.3 vs
- * 16.1 us; T = 128: 22 vs 76 us). Constraints: 1 <= T <= 256,
+ * faster up to 8 tokens and this path from 12 on (T = 32: 9.9 vs 15.8 us;
+ * T = 128: 19.4 vs 74.7 us), so wo_a_grouped itself takes this path above 8
+ * tokens. Constraints: 1 <= T <= 256,
  * d_nope = 448, d_rope = 64, R % 128 == 0, else MX_ERR_UNSUPPORTED. A position
  * outside [0, max_pos) reads cache row 0 and is reported by mx_device_status,
  * as in wo_a_grouped. */

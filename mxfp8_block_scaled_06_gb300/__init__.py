@@ -416,9 +416,11 @@ def _wo_a_resident(h: Handle, x, positions, cos_sin, w, w_scales):
 def wo_a_grouped(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,
                  heads_per_group: int, o_lora_rank: int, d_nope: int = 448, d_rope: int = 64,
                  q=None, q_scales=None, debug: bool = False, early_trigger: bool = False,
-                 stream=None) -> dict:
+                 z: bool = False, stream=None) -> dict:
     """x: bf16 [T, heads, d_nope + d_rope] (token stride x.stride(0)); returns the
-    MXFP8 activation (q, q_scales) for wo_b, plus debug tensors if asked."""
+    MXFP8 activation (q, q_scales) for wo_b, plus debug tensors if asked: z (bf16
+    before requantization) with z or debug, the quantized activation with debug
+    (which keeps the call on the fused kernel at every T)."""
     import torch
     t, kall, cols = _wo_a_inputs(x, positions, cos_sin, w, w_scales, n_groups, heads_per_group,
                                  o_lora_rank, d_nope, d_rope)
@@ -426,7 +428,7 @@ def wo_a_grouped(h: Handle, x, positions, cos_sin, w, w_scales, n_groups: int,
     q = _empty_u8((t, cols), dev) if q is None else _matrix("q", q, _codes_types(), t, cols)
     q_scales = (_empty_u8((_sbytes(t, cols),), dev) if q_scales is None else
                 _flat("q_scales", q_scales, _scale_types(), _sbytes(t, cols)))
-    dz = torch.empty((t, cols), dtype=torch.bfloat16, device=dev) if debug else None
+    dz = torch.empty((t, cols), dtype=torch.bfloat16, device=dev) if debug or z else None
     dxq = _empty_u8((t, kall), dev) if debug else None
     dxs = _empty_u8((t, kall // 32), dev) if debug else None
     _wo_a_resident(h, x, positions, cos_sin, w, w_scales)

@@ -18,7 +18,7 @@ LIB = os.path.join(HERE, "libmx.so")
 # stamps of every GEMM launch, read back with mx_timeline_read); diagnostic only.
 TIMELINE_LIB = os.path.join(HERE, "libmx_timeline.so")
 TIMELINE_BUILD = os.path.join(HERE, "_build_timeline")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "wo_a.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "wo_a.cu", "chain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

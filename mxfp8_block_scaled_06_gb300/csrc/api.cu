@@ -28,6 +28,10 @@ struct mx_handle {
   int device;
   int sm_count;
   int* d_status;
+  unsigned* d_chain;   // persistent chain kernel's counters (kChainCounters words)
+  int chain_clusters;  // clusters of 8 CTAs it may use (0: the three-launch path only)
+  uint8_t* d_woa;      // wo_a_grouped's two-launch activation (kWoaScratchBytes)
+  float* d_ssq;        // mx_gemm_chain_norm's block sums of squares (kSsqBytes)
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   TmapEntry tmaps[kTmapCache];
   int tmap_count;
@@ -37,6 +41,21 @@ struct mx_handle {
   int tl_next;               // GEMM launches recorded since the last reset
 #endif
 };
+// wo_a_grouped above kWoaFusedMaxTokens tokens runs the two-launch form and
+// keeps its quantized activation in the handle: codes [T, G*H*D], then the
+// swizzled scales at the next 256-byte boundary. Room for T = 128 tokens of
+// G*H*D = 65536 (8 MiB of codes, 256 KiB of scales).
+constexpr size_t kWoaScratchBytes = (size_t{8} << 20) + (size_t{256} << 10) + 256;
+// Measured on GB300 (4 groups x 1024 rows, 8 heads of 512): the fused kernel
+// is faster up to 8 tokens (7.5 against 8.1 us), the two launches from 12 on
+// (8.3 against 8.4 us; 19 against 75 us at 128 tokens).
+constexpr int kWoaFusedMaxTokens = 8;
+// mx_gemm_chain_norm applies the RMS norm in G2's prologue up to this many rows
+// (measured on GB300 with N1 = 2048, qr 1536, N2 = 8192, N3 = 5120; beyond, G2's
+// CTAs each quantizing their K-range of every row cost more than a launch).
+constexpr int kNormFusedMaxRows = 16;
+// the block sums of squares G1 hands to G2 there: [M, g1_cols / 32] floats
+constexpr size_t kSsqBytes = size_t{64} << 10;
 #ifdef MX_TIMELINE
 constexpr int kTimelineLaunches = 256;
 constexpr size_t kTimelineBytes =
@@ -94,32 +113,40 @@ int validate_gemm(const mx_handle* h, int M, int N, int K, const void* a, const 
   return MX_OK;
 }
 
+// One GEMM launch, prepared (plan, tensor maps, arguments) before anything is
+// enqueued, so that a call of several launches can fail before its first.
+struct GemmLaunch {
+  mx::GemmPlan plan;
+  CUtensorMap tm_w, tm_a;
+  mx::GemmArgs args;
+};
+
 // a = MXFP8 activations (+ a_scales), or x = bf16 activations with row stride
 // ldx (quantized inside the kernel); exactly one of the two is non-null.
 // groups > 1: a is [M, groups * K] and the weight tiles of group g (N / groups
 // rows each) contract its K-slice g.
-int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
-                const void* w, const void* w_scales, void* out, uint8_t* q, uint8_t* q_scales,
-                int q_cols, bool pdl, cudaStream_t stream, const void* x = nullptr, long ldx = 0,
-                int groups = 1) {
-  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, x != nullptr);
-  CUtensorMap tm_w, tm_a;
-  int rc = make_tmap(h, &tm_w, w, N, K, 128);
+int gemm_prepare(mx_handle* h, GemmLaunch* L, int M, int N, int K, const void* a,
+                 const void* a_scales, const void* w, const void* w_scales, void* out, uint8_t* q,
+                 uint8_t* q_scales, int q_cols, const void* x = nullptr, long ldx = 0,
+                 int groups = 1, const mx::GemmNorm* norm = nullptr) {
+  L->plan = mx::plan_gemm(M, N, K, h->sm_count, x != nullptr, norm != nullptr);
+  int rc = make_tmap(h, &L->tm_w, w, N, K, 128);
   if (rc != MX_OK) return rc;
   if (x != nullptr) {
-    tm_a = tm_w;  // not read by the fused kernel
+    L->tm_a = L->tm_w;  // not read by the fused kernel
   } else {
-    rc = make_tmap(h, &tm_a, a, M, static_cast<long>(K) * groups, plan.mtile);
+    rc = make_tmap(h, &L->tm_a, a, M, static_cast<long>(K) * groups, L->plan.mtile);
     if (rc != MX_OK) return rc;
   }
-  mx::GemmArgs args = {};
+  mx::GemmArgs& args = L->args;
+  args = mx::GemmArgs{};
   args.M = M;
   args.N = N;
   args.K = K;
-  args.mtile = plan.mtile;
-  args.stages = plan.stages;
+  args.mtile = L->plan.mtile;
+  args.stages = L->plan.stages;
   args.nchunks = K / 128;
-  args.tmem_cols = plan.tmem_cols;
+  args.tmem_cols = L->plan.tmem_cols;
   args.a_scales = static_cast<const uint8_t*>(a_scales);
   args.w_scales = static_cast<const uint8_t*>(w_scales);
   args.x = static_cast<const uint16_t*>(x);
@@ -130,13 +157,91 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
   args.q = q;
   args.q_scales = q_scales;
   args.q_cols = q_cols;
+  if (norm != nullptr) args.norm = *norm;
   args.status = h->d_status;
+  return MX_OK;
+}
+
+int gemm_run(mx_handle* h, GemmLaunch* L, bool pdl, cudaStream_t stream) {
+#ifdef MX_TIMELINE
+  L->args.tl = nullptr;
+  if (h->d_tl != nullptr && (L->args.N / 128) * L->plan.splits <= mx::kTimelineCtas &&
+      h->tl_next < kTimelineLaunches)
+    L->args.tl = h->d_tl + static_cast<size_t>(h->tl_next++) * mx::kTimelineCtas * mx::kTimelineSlots;
+#else
+  (void)h;
+#endif
+  return cuda_status(mx::launch_gemm(L->tm_w, L->tm_a, L->args, L->plan, pdl, stream));
+}
+
+int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
+                const void* w, const void* w_scales, void* out, uint8_t* q, uint8_t* q_scales,
+                int q_cols, bool pdl, cudaStream_t stream, const void* x = nullptr, long ldx = 0,
+                int groups = 1) {
+  GemmLaunch L;
+  const int rc = gemm_prepare(h, &L, M, N, K, a, a_scales, w, w_scales, out, q, q_scales, q_cols, x,
+                              ldx, groups);
+  return rc != MX_OK ? rc : gemm_run(h, &L, pdl, stream);
+}
+
+// The chain in one persistent kernel (chain.cu), when MX_CHAIN_PERSISTENT=1 and
+// its plan exists (up to 16 rows, K splits of each projection's GEMM plan at
+// most 8, enough resident clusters). Measured on GB300 it is slower than the
+// three launches (33 vs 19 us at one row: its weight ring fills during each
+// projection's dependency wait and every hand-off is a chain of ~0.5 us
+// latencies), so the three launches are the default.
+// Returns MX_OK after launching, MX_ERR_UNSUPPORTED when the three-launch path
+// must serve the call, or an error before any launch.
+int chain_persistent(mx_handle* h, int M, const void* a1, const void* a1_scales, const mx_weight w[3],
+                     int g1_cols, void* a2, void* a2_scales, void* a3, void* a3_scales, void* out,
+                     void* out1, void* out2, cudaStream_t stream) {
+  const char* e = getenv("MX_CHAIN_PERSISTENT");
+  if (e == nullptr || atoi(e) != 1) return MX_ERR_UNSUPPORTED;
+  if (h->chain_clusters < 1) return MX_ERR_UNSUPPORTED;
+  mx::ChainArgs args = {};
+  const void* acts[3] = {a1, a2, a3};
+  const void* act_scales[3] = {a1_scales, a2_scales, a3_scales};
+  void* outs[3] = {out1, out2, out};
+  uint8_t* qs[3] = {static_cast<uint8_t*>(a2), static_cast<uint8_t*>(a3), nullptr};
+  uint8_t* qscales[3] = {static_cast<uint8_t*>(a2_scales), static_cast<uint8_t*>(a3_scales), nullptr};
+  const int qcols[3] = {g1_cols, w[1].n, 0};
+  for (int p = 0; p < 3; ++p) {
+    mx::ChainProj& P = args.proj[p];
+    P.w_scales = static_cast<const uint8_t*>(w[p].w_scales);
+    P.a_scales = static_cast<const uint8_t*>(act_scales[p]);
+    P.n = w[p].n;
+    P.k = w[p].k;
+    P.splits = mx::plan_gemm(M, w[p].n, w[p].k, h->sm_count).splits;
+    P.out = outs[p];
+    P.q = qs[p];
+    P.q_scales = qscales[p];
+    P.q_cols = qcols[p];
+  }
+  args.plan = mx::plan_chain(M, args.proj, h->chain_clusters);
+  if (!args.plan.ok) return MX_ERR_UNSUPPORTED;
+  args.cnt_off[0] = 4;
+  args.cnt_off[1] = 4 + w[0].n / 128;
+  if (args.cnt_off[1] + w[1].n / 128 > mx::kChainCounters) return MX_ERR_UNSUPPORTED;
+  args.M = M;
+  args.mtile = (M + 15) & ~15;
+  args.nsfb = 1;
+  args.counters = h->d_chain;
+  args.status = h->d_status;
+  CUtensorMap maps[6];
+  const int act_k[3] = {w[0].k, g1_cols, w[1].n};
+  for (int p = 0; p < 3; ++p) {
+    int rc = make_tmap(h, &maps[p], w[p].w, w[p].n, w[p].k, 128);
+    if (rc != MX_OK) return rc;
+    rc = make_tmap(h, &maps[3 + p], acts[p], M, act_k[p], args.mtile);
+    if (rc != MX_OK) return rc;
+  }
 #ifdef MX_TIMELINE
   args.tl = nullptr;
-  if (h->d_tl != nullptr && (N / 128) * plan.splits <= mx::kTimelineCtas && h->tl_next < kTimelineLaunches)
+  if (h->d_tl != nullptr && mx::kChainCluster * args.plan.clusters <= mx::kTimelineCtas &&
+      h->tl_next < kTimelineLaunches)
     args.tl = h->d_tl + static_cast<size_t>(h->tl_next++) * mx::kTimelineCtas * mx::kTimelineSlots;
 #endif
-  return cuda_status(mx::launch_gemm(tm_w, tm_a, args, plan, pdl, stream));
+  return cuda_status(mx::launch_chain(maps, args, stream));
 }
 
 }  // namespace
@@ -173,18 +278,29 @@ int mx_create(mx_handle** out, int device) {
     } else {
       h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       if (mx::set_gemm_attributes() != cudaSuccess || mx::set_wo_a_attributes() != cudaSuccess ||
+          mx::set_chain_attributes() != cudaSuccess ||
           cudaMalloc(&h->d_status, 16) != cudaSuccess ||
           cudaMemset(h->d_status, 0, 16) != cudaSuccess ||
+          cudaMalloc(&h->d_chain, mx::kChainCounters * sizeof(unsigned)) != cudaSuccess ||
+          cudaMemset(h->d_chain, 0, mx::kChainCounters * sizeof(unsigned)) != cudaSuccess ||
+          cudaMalloc(&h->d_woa, kWoaScratchBytes) != cudaSuccess ||
+          cudaMalloc(&h->d_ssq, kSsqBytes) != cudaSuccess ||
 #ifdef MX_TIMELINE
           cudaMalloc(&h->d_tl, kTimelineBytes) != cudaSuccess ||
           cudaMemset(h->d_tl, 0, kTimelineBytes) != cudaSuccess ||
 #endif
           cudaDeviceSynchronize() != cudaSuccess)
         rc = MX_ERR_CUDA;
+      // every CTA of the chain kernel must be resident at once: the largest
+      // number of its clusters that fit (16 at most are used)
+      if (rc == MX_OK) h->chain_clusters = std::min(16, mx::chain_max_clusters());
     }
   }
   if (rc != MX_OK && h != nullptr) {
     if (h->d_status) cudaFree(h->d_status);
+    if (h->d_chain) cudaFree(h->d_chain);
+    if (h->d_woa) cudaFree(h->d_woa);
+    if (h->d_ssq) cudaFree(h->d_ssq);
     delete h;
     h = nullptr;
   }
@@ -199,6 +315,9 @@ int mx_destroy(mx_handle* h) {
   cudaGetDevice(&prev);
   cudaSetDevice(h->device);
   cudaFree(h->d_status);
+  cudaFree(h->d_chain);
+  cudaFree(h->d_woa);
+  cudaFree(h->d_ssq);
 #ifdef MX_TIMELINE
   cudaFree(h->d_tl);
 #endif
@@ -288,14 +407,21 @@ int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, co
   if ((debug_out1 && !aligned(debug_out1, 16)) || (debug_out2 && !aligned(debug_out2, 16)))
     return MX_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = gemm_launch(h, M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, debug_out1,
-                   static_cast<uint8_t*>(a2), static_cast<uint8_t*>(a2_scales), g1_cols, true, s);
-  if (rc != MX_OK) return rc;
-  rc = gemm_launch(h, M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
-                   static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n, true, s);
-  if (rc != MX_OK) return rc;
-  return gemm_launch(h, M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
-                     nullptr, 0, true, s);
+  rc = chain_persistent(h, M, a1, a1_scales, w, g1_cols, a2, a2_scales, a3, a3_scales, out,
+                        debug_out1, debug_out2, s);
+  if (rc != MX_ERR_UNSUPPORTED) return rc;
+  // three launches, every tensor map encoded before the first
+  GemmLaunch L[3];
+  rc = gemm_prepare(h, &L[0], M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, debug_out1,
+                    static_cast<uint8_t*>(a2), static_cast<uint8_t*>(a2_scales), g1_cols);
+  if (rc == MX_OK)
+    rc = gemm_prepare(h, &L[1], M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
+                      static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n);
+  if (rc == MX_OK)
+    rc = gemm_prepare(h, &L[2], M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
+                      nullptr, 0);
+  for (int i = 0; i < 3 && rc == MX_OK; ++i) rc = gemm_run(h, &L[i], true, s);
+  return rc;
 }
 
 int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scales,
@@ -318,20 +444,75 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
   if (out == nullptr || !aligned(out, 16) || !aligned(out1, 16) || !aligned(norm_weight, 16) ||
       (debug_y && !aligned(debug_y, 16)) || (debug_out2 && !aligned(debug_out2, 16)))
     return MX_ERR_INVALID_ARG;
+  // Up to kNormFusedMaxRows rows G2 applies the norm in its prologue (three
+  // launches); beyond, every one of G2's CTAs would repeat the RMS pass over all
+  // rows, and the stand-alone norm kernel between G1 and G2 is faster.
+  const bool fused = M <= kNormFusedMaxRows &&
+                     static_cast<size_t>(M) * (g1_cols / 32) * sizeof(float) <= kSsqBytes &&
+                     mx::plan_gemm(M, w[1].n, w[1].k, h->sm_count, true, true).smem <= mx::kMaxDynamicSmem;
+  const mx::GemmNorm norm{static_cast<const uint16_t*>(norm_weight), eps, h->d_ssq,
+                          static_cast<uint16_t*>(debug_y), static_cast<uint8_t*>(a2),
+                          static_cast<uint8_t*>(a2_scales)};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // G1 -> bf16 out1 (qr | kv); RMS norm of qr + MX quantize -> a2; G2 (+ requant) -> a3; G3
-  rc = gemm_launch(h, M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, out1, nullptr,
-                   nullptr, 0, true, s);
+  // G1 -> bf16 out1 (qr | kv) and, fused, qr's block sums of squares; G2 reads
+  // qr in bf16, normalizes and quantizes it in its prologue (writing a2 on the
+  // way) or reads a2 written by the norm kernel, and requantizes into a3; G3.
+  // Every tensor map is encoded before the first launch.
+  GemmLaunch L[3];
+  rc = gemm_prepare(h, &L[0], M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, out1, nullptr,
+                    nullptr, 0);
+  if (fused) {
+    L[0].args.ssq_out = h->d_ssq;
+    L[0].args.ssq_cols = g1_cols;
+  }
+  if (rc == MX_OK && fused)
+    rc = gemm_prepare(h, &L[1], M, w[1].n, w[1].k, nullptr, nullptr, w[1].w, w[1].w_scales,
+                      debug_out2, static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n,
+                      out1, w[0].n, 1, &norm);
+  else if (rc == MX_OK)
+    rc = gemm_prepare(h, &L[1], M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
+                      static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n);
+  if (rc == MX_OK)
+    rc = gemm_prepare(h, &L[2], M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
+                      nullptr, 0);
   if (rc != MX_OK) return rc;
-  rc = cuda_status(mx::launch_rmsnorm_quantize_rows(out1, w[0].n, M, g1_cols, norm_weight, eps,
-                                                    debug_y, a2, a2_scales, 1, s));
+  rc = gemm_run(h, &L[0], true, s);
   if (rc != MX_OK) return rc;
-  rc = gemm_launch(h, M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
-                   static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n, true, s);
+  if (!fused) {
+    rc = cuda_status(mx::launch_rmsnorm_quantize_rows(out1, w[0].n, M, g1_cols, norm_weight, eps,
+                                                      debug_y, a2, a2_scales, 1, s));
+    if (rc != MX_OK) return rc;
+  }
+  rc = gemm_run(h, &L[1], true, s);
   if (rc != MX_OK) return rc;
-  return gemm_launch(h, M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
-                     nullptr, 0, true, s);
+  return gemm_run(h, &L[2], true, s);
 }
+
+namespace {
+
+// WO-A as two launches (inverse RoPE + MX quantization into xq, then one grouped
+// GEMM with the requantization in its epilogue). The arguments are validated by
+// the caller; returns MX_ERR_UNSUPPORTED before any launch when the GEMM has no
+// plan for the shape.
+int woa_two_launch(mx_handle* h, int T, const void* x, long ldx, const int64_t* positions,
+                   const float* cos_sin, int max_pos, const void* w, const void* w_scales, int G,
+                   int H, int d_nope, int d_rope, int R, void* xq, void* xq_scales, void* z,
+                   void* q, void* q_scales, cudaStream_t s) {
+  const int D = d_nope + d_rope;
+  const long kx = static_cast<long>(G) * H * D;  // the activation's K (all groups)
+  if (kx > (1L << 30) || mx::plan_gemm(T, G * R, H * D, h->sm_count).smem > mx::kMaxDynamicSmem)
+    return MX_ERR_UNSUPPORTED;
+  // 1. inverse RoPE + MX quantize of all heads -> xq (swizzled scales over G*H*D)
+  const mx::RopeArgs rope{positions, cos_sin, max_pos, D, d_nope, h->d_status};
+  int rc = cuda_status(mx::launch_quantize_rows(x, ldx, T, static_cast<int>(kx), xq, xq_scales, 1, s, rope));
+  if (rc != MX_OK) return rc;
+  // 2. one grouped GEMM: tile rows of group g contract xq's K-slice g; z rounded
+  //    to bf16 and requantized in the epilogue
+  return gemm_launch(h, T, G * R, H * D, xq, xq_scales, w, w_scales, z, static_cast<uint8_t*>(q),
+                     static_cast<uint8_t*>(q_scales), G * R, true, s, nullptr, 0, G);
+}
+
+}  // namespace
 
 int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* positions,
                  const float* cos_sin, int max_pos, const void* w, const void* w_scales, int G,
@@ -351,6 +532,19 @@ int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* po
     return MX_ERR_INVALID_ARG;
   if ((debug_z && !aligned(debug_z, 16)) || (debug_xq && !aligned(debug_xq, 16)))
     return MX_ERR_INVALID_ARG;
+  // Above kWoaFusedMaxTokens the two launches are faster: every CTA of the fused
+  // kernel quantizes its group's whole activation slice, which then outweighs
+  // the weight stream. They need the handle's scratch for the activation, so
+  // the fused kernel serves calls that ask for its debug copy of it.
+  const long kx = static_cast<long>(G) * H * D;
+  const size_t codes = (static_cast<size_t>(T) * kx + 255) & ~size_t{255};
+  if (T > kWoaFusedMaxTokens && debug_xq == nullptr && debug_xs == nullptr && kx <= (1L << 24) &&
+      codes + mx_scale_bytes(T, static_cast<int>(kx)) <= kWoaScratchBytes) {
+    rc = woa_two_launch(h, T, x, ldx, positions, cos_sin, max_pos, w, w_scales, G, H, d_nope, d_rope,
+                        R, h->d_woa, h->d_woa + codes, debug_z, q, q_scales,
+                        static_cast<cudaStream_t>(stream));
+    if (rc != MX_ERR_UNSUPPORTED) return rc;
+  }
   const mx::WoaPlan plan = mx::plan_wo_a(T, G, H, R, h->sm_count);
   CUtensorMap tm_w;
   rc = make_tmap(h, &tm_w, w, G * R, H * D, 128);
@@ -399,17 +593,8 @@ int wo_a_grouped_unfused(mx_handle* h, int T, const void* x, long ldx, const int
       !aligned(xq_scales, 16) || !aligned(q, 16) || !aligned(q_scales, 16) ||
       !aligned(cos_sin, 16) || !aligned(positions, 8) || (z && !aligned(z, 16)))
     return MX_ERR_INVALID_ARG;
-  if (kx > (1L << 30) || mx::plan_gemm(T, G * R, H * D, h->sm_count).smem > mx::kMaxDynamicSmem)
-    return MX_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // 1. inverse RoPE + MX quantize of all heads -> xq (swizzled scales over G*H*D)
-  const mx::RopeArgs rope{positions, cos_sin, max_pos, D, d_nope, h->d_status};
-  rc = cuda_status(mx::launch_quantize_rows(x, ldx, T, static_cast<int>(kx), xq, xq_scales, 1, s, rope));
-  if (rc != MX_OK) return rc;
-  // 2. one grouped GEMM: tile rows of group g contract xq's K-slice g; z rounded
-  //    to bf16 and requantized in the epilogue
-  return gemm_launch(h, T, G * R, H * D, xq, xq_scales, w, w_scales, z, static_cast<uint8_t*>(q),
-                     static_cast<uint8_t*>(q_scales), G * R, true, s, nullptr, 0, G);
+  return woa_two_launch(h, T, x, ldx, positions, cos_sin, max_pos, w, w_scales, G, H, d_nope, d_rope,
+                        R, xq, xq_scales, z, q, q_scales, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------ chain without allocation
@@ -473,6 +658,9 @@ int mx_device_status(mx_handle* h, int* status) {
   if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MX_ERR_CUDA;
   if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return MX_ERR_CUDA;
+  // a failed chain call leaves its counters inconsistent: start them afresh
+  if (v != 0 && cudaMemset(h->d_chain, 0, mx::kChainCounters * sizeof(unsigned)) != cudaSuccess)
+    return MX_ERR_CUDA;
   *status = (v & 1) ? MX_ERR_TIMEOUT : (v & 2) ? MX_ERR_INVALID_ARG : MX_OK;
   return MX_OK;
 }

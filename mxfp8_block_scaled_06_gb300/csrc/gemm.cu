@@ -51,7 +51,9 @@ constexpr int kThreads = 128;
 // written to p.tl[cta * kTimelineSlots + slot]: 0 entry, 1 set-up done, 2 first
 // weight box issued, 3 weight scale tiles landed, 4 grid-dependency wait
 // returned, 5 first chunk landed, 6 accumulator complete, 7 reduction barrier
-// passed, 8 reduction done, 9 exit, 10 SM id, 11 chunks in the K-range.
+// passed, 8 reduction done, 9 exit, 10 SM id, 11 chunks in the K-range,
+// 12 bf16 activations quantized, 13 RMS of the rows done, 14 first row batch
+// landed (12-14: in-kernel quantization only).
 #ifdef MX_TIMELINE
 #define MX_TL(slot, v)                                                             \
   do {                                                                             \
@@ -76,12 +78,15 @@ constexpr uint32_t kSfTileBytes = 512;       // one 128x4 scale tile
 // K-range (loaded once), then the mbarriers. With bf16 activations quantized in
 // the kernel (`fused`), the ring holds weight boxes only and the activation
 // tiles of the whole K-range are resident, after the scale tiles, followed by a
-// staging area for up to kRowBatch bf16 rows of the K-range.
+// staging area for up to kRowBatch bf16 rows of the K-range. With the RMS norm
+// (norm_blocks = K/32) follow the norm weight's K-range, the staged rows'
+// per-block sums of squares and the rows' reciprocal RMS (a float per tile row).
 constexpr int kRowBatch = 32;
 struct Layout {
-  uint32_t a_bytes, stage_bytes, ring_bytes, sfa_bytes, sfb_bytes, act, xraw, bars;
+  uint32_t a_bytes, stage_bytes, ring_bytes, sfa_bytes, sfb_bytes, act, xraw, gam, ssq, inv, bars;
   int stages, nsfb, nmax;
-  __host__ __device__ Layout(int mtile, int stages_, int nmax_, bool fused = false, int xrows = 0) {
+  __host__ __device__ Layout(int mtile, int stages_, int nmax_, bool fused = false, int xrows = 0,
+                             int norm_blocks = 0) {
     stages = stages_;
     nmax = nmax_;
     nsfb = (mtile + 127) / 128;
@@ -92,7 +97,11 @@ struct Layout {
     sfb_bytes = static_cast<uint32_t>(nmax * nsfb) * kSfTileBytes;
     act = (ring_bytes + sfa_bytes + sfb_bytes + 1023u) & ~1023u;
     xraw = act + (fused ? static_cast<uint32_t>(nmax) * a_bytes : 0u);
-    bars = xraw + (fused ? static_cast<uint32_t>(xrows * nmax) * 256u : 0u);
+    gam = xraw + (fused ? static_cast<uint32_t>(xrows * nmax) * 256u : 0u);
+    const bool norm = fused && norm_blocks > 0;
+    ssq = gam + (norm ? static_cast<uint32_t>(nmax) * 256u : 0u);
+    inv = ssq + (norm ? static_cast<uint32_t>(xrows * norm_blocks) * 4u : 0u);
+    bars = inv + (norm ? static_cast<uint32_t>(mtile) * 4u : 0u);
   }
   __host__ __device__ uint32_t w_off(int s) const { return s * stage_bytes; }
   __host__ __device__ uint32_t a_off(int s) const { return s * stage_bytes + kWTileBytes; }
@@ -126,7 +135,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int stages = p.stages;
   // grouped activations: this tile's group reads its own K-slice of A
   const int a_k0 = p.group_tiles > 0 ? (tile / p.group_tiles) * p.K : 0;
-  const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S, kFusedA, min(p.M, kRowBatch));
+  const bool norm = kFusedA && p.norm.gamma != nullptr;
+  const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S, kFusedA, min(p.M, kRowBatch),
+                 norm ? p.K / 32 : 0);
   const int nsfb = L.nsfb;
   if (threadIdx.x == 0) MX_TL(0, globaltimer());
 
@@ -210,6 +221,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) MX_TL(10, tl_smid());
   if (threadIdx.x == 0) MX_TL(11, static_cast<unsigned long long>(n));
 #endif
+  if constexpr (kFusedA) {
+    // shared memory only, so before the wait: zero rows [M, mtile) of every
+    // activation chunk tile, and the activation scale tiles
+    for (int idx = threadIdx.x; idx < n * (p.mtile - p.M) * 8; idx += kThreads) {
+      const int i = idx / ((p.mtile - p.M) * 8), rem = idx % ((p.mtile - p.M) * 8);
+      const int m = p.M + rem / 8;
+      *reinterpret_cast<uint4*>(base_ptr + L.act + i * L.a_bytes + m * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    for (int idx = threadIdx.x; idx < n * nsfb * 32; idx += kThreads)
+      *reinterpret_cast<uint4*>(base_ptr + L.sfb_off(idx / (n * 32), 0) + (idx % (n * 32)) * 16) =
+          make_uint4(0, 0, 0, 0);
+  }
   pdl_wait();
   if (threadIdx.x == 0) MX_TL(4, globaltimer());
 
@@ -228,42 +252,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // bf16 rows of the CTA's K-range -> MXFP8 codes in the 128-byte-swizzled
-    // K-major operand layout and the 128x4 scale tiles, in shared memory
+    // K-major operand layout and the 128x4 scale tiles, in shared memory (rows
+    // [M, mtile) and the scale tiles were zeroed before the wait)
     const uint32_t at = L.a_bytes;
-    for (int idx = threadIdx.x; idx < n * (p.mtile - p.M) * 8; idx += kThreads) {
-      // zero rows [M, mtile) of every chunk tile
-      const int i = idx / ((p.mtile - p.M) * 8), rem = idx % ((p.mtile - p.M) * 8);
-      const int m = p.M + rem / 8;
-      *reinterpret_cast<uint4*>(base_ptr + L.act + i * at + m * 128 + (rem % 8) * 16) =
-          make_uint4(0, 0, 0, 0);
-    }
-    for (int idx = threadIdx.x; idx < n * nsfb * 32; idx += kThreads)
-      *reinterpret_cast<uint4*>(base_ptr + L.sfb_off(idx / (n * 32), 0) + (idx % (n * 32)) * 16) =
-          make_uint4(0, 0, 0, 0);
-    const int units_per_row = n * 16;  // 8-element units in the K-range
+    float* const row_inv = reinterpret_cast<float*>(base_ptr + L.inv);
+    const bool norm_out = norm && tile == 0;  // tile 0 writes y and the activation
+    const int nblk = p.K >> 5;                // 32-blocks of a whole row (the norm's sum)
+    const int units_per_row = n * 16;         // 8-element units in the K-range
     for (int r0 = 0, batch = 0; r0 < p.M; r0 += kRowBatch, ++batch) {
+      // every thread reads the flag after the previous batch's barrier: once a
+      // wait has expired no further row batch is requested
+      if (*abort_flag != 0) break;
       const int rb = min(kRowBatch, p.M - r0);
+      const bool gam = norm && batch == 0;  // the norm weight's K-range comes with batch 0
       if (warp == 3) {
-        // one lane per row: each row's K-range is contiguous
-        if (lane == 0) mbar_expect_tx(x_bar, static_cast<uint32_t>(rb * n) * 256u);
+        // one lane per row: each row's K-range is contiguous; with the norm, lane
+        // 31 also copies the batch's block sums of squares (contiguous rows), and
+        // lane 30 the norm weight's K-range with the first batch
+        const uint32_t ssq_bytes = static_cast<uint32_t>(rb * nblk) * 4u;
+        if (lane == 0)
+          mbar_expect_tx(x_bar, static_cast<uint32_t>(rb * n) * 256u + (norm ? ssq_bytes : 0u) +
+                                    (gam ? static_cast<uint32_t>(n) * 256u : 0u));
         __syncwarp();
         if (lane < rb)
           bulk_load(base + L.xraw + lane * L.nmax * 256,
                     p.x + static_cast<size_t>(r0 + lane) * p.ldx + static_cast<size_t>(c_begin) * 128,
                     static_cast<uint32_t>(n) * 256u, x_bar, pol_a);
+        if (norm && lane == 31)
+          bulk_load(base + L.ssq, p.norm.ssq + static_cast<size_t>(r0) * nblk, ssq_bytes, x_bar, pol_a);
+        if (gam && lane == 30)
+          bulk_load(base + L.gam, p.norm.gamma + static_cast<size_t>(c_begin) * 128,
+                    static_cast<uint32_t>(n) * 256u, x_bar, pol_a);
         x_batches = batch + 1;
       }
+      if (gam && norm_out && p.norm.a_q_scales != nullptr) {
+        // padding rows [M, ceil128(M)) of the K-range's scale columns
+        const int mpad = (p.M + 127) & ~127;
+        for (int idx = threadIdx.x; idx < (mpad - p.M) * n * 4; idx += kThreads)
+          p.norm.a_q_scales[swz_offset(p.M + idx / (n * 4), c_begin * 4 + idx % (n * 4), nblk)] = 0;
+      }
       if (!mbar_wait(x_bar, batch & 1)) fail();
+      if (batch == 0 && threadIdx.x == 0) MX_TL(14, globaltimer());
+      if (norm) {
+        // reciprocal RMS of the batch's rows, one thread per row: the blocks'
+        // sums of squares added in block order, as the stand-alone norm kernel does
+        if (threadIdx.x < rb) {
+          const float* const sq = reinterpret_cast<const float*>(base_ptr + L.ssq) + threadIdx.x * nblk;
+          float ss = 0.f;
+#pragma unroll 8
+          for (int b = 0; b < nblk; ++b) ss = __fadd_rn(ss, sq[b]);
+          row_inv[r0 + threadIdx.x] =
+              __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(p.K)), p.norm.eps)));
+        }
+        __syncthreads();
+        if (batch == 0 && threadIdx.x == 0) MX_TL(13, globaltimer());
+      }
       const int total = rb * units_per_row;
+      const bool go = *abort_flag == 0;
+      // unit u = b0 + threadIdx.x is (row, ul), advanced by kThreads units a pass
+      int row = threadIdx.x / units_per_row, ul = threadIdx.x % units_per_row;
+      const int drow = kThreads / units_per_row, dul = kThreads % units_per_row;
       for (int b0 = 0; b0 < total; b0 += kThreads) {
-        const int u = b0 + threadIdx.x;
-        const bool valid = u < total && *abort_flag == 0;
-        const int row = u / units_per_row;
-        const int ul = u % units_per_row;
+        const bool valid = go && b0 + static_cast<int>(threadIdx.x) < total;
         const int blk = ul >> 2;  // 32-block within the K-range
         float v[8];
-        float amax = 0.f;
-        uint32_t nonfinite = 0;
+        uint32_t amax_bits = 0;  // max |v| as bits: at or above Inf's bits when any is Inf or NaN
         if (valid) {
           const uint4 raw = *reinterpret_cast<const uint4*>(base_ptr + L.xraw + row * L.nmax * 256 + ul * 16);
           const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -272,24 +325,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[2 * e] = __uint_as_float(w4[e] << 16);
             v[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
           }
+          if (norm) {
+            // y = bf16((x * inv_rms) * gamma), as the stand-alone norm kernel
+            const float inv = row_inv[r0 + row];
+            const int kg = c_begin * 128 + ul * 8;
+            const uint4 graw = *reinterpret_cast<const uint4*>(base_ptr + L.gam + ul * 16);
+            const uint32_t g4[4] = {graw.x, graw.y, graw.z, graw.w};
+            uint32_t packed[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            amax = fmaxf(amax, fabsf(v[e]));
-            nonfinite |= !isfinite(v[e]);
+            for (int e = 0; e < 4; ++e) {
+              const float a = __fmul_rn(__fmul_rn(v[2 * e], inv), __uint_as_float(g4[e] << 16));
+              const float b = __fmul_rn(__fmul_rn(v[2 * e + 1], inv), __uint_as_float(g4[e] & 0xFFFF0000u));
+              const uint32_t ha = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+              const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+              packed[e] = ha | (hb << 16);
+              v[2 * e] = __uint_as_float(ha << 16);
+              v[2 * e + 1] = __uint_as_float(hb << 16);
+            }
+            if (norm_out && p.norm.y != nullptr)
+              *reinterpret_cast<uint4*>(p.norm.y + static_cast<size_t>(r0 + row) * p.K + kg) =
+                  make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7FFFFFFFu);
         }
         // the four units of a 32-block sit in four consecutive lanes
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-        nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 1);
-        nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, 2);
+        amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, 1));
+        amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, 2));
         if (valid) {
           uint32_t sbyte, lo, hi;
-          if (nonfinite) {
+          if (amax_bits >= 0x7F800000u) {
             sbyte = 0xFFu;
             lo = hi = 0x7F7F7F7Fu;
           } else {
-            sbyte = mx_scale_byte(amax);
+            sbyte = mx_scale_byte(__uint_as_float(amax_bits));
             const float f = mx_inv_scale(sbyte);
             lo = cvt_e4m3x2(v[0] * f, v[1] * f) | (cvt_e4m3x2(v[2] * f, v[3] * f) << 16);
             hi = cvt_e4m3x2(v[4] * f, v[5] * f) | (cvt_e4m3x2(v[6] * f, v[7] * f) << 16);
@@ -303,12 +372,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((ul & 3) == 0)
             base_ptr[L.sfb_off(m >> 7, ci) + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (blk & 3)] =
                 static_cast<uint8_t>(sbyte);
+          if (norm_out && p.norm.a_q != nullptr) {
+            const int kg = c_begin * 128 + ul * 8;
+            *reinterpret_cast<uint2*>(p.norm.a_q + static_cast<size_t>(m) * p.K + kg) = make_uint2(lo, hi);
+            if ((ul & 3) == 0) p.norm.a_q_scales[swz_offset(m, kg >> 5, p.K >> 5)] = static_cast<uint8_t>(sbyte);
+          }
+        }
+        row += drow;
+        ul += dul;
+        if (ul >= units_per_row) {
+          ul -= units_per_row;
+          ++row;
         }
       }
       __syncthreads();  // the next batch reuses the staging rows
     }
     fence_proxy_async_smem();  // written by the threads, read by the tensor cores
     __syncthreads();
+    if (threadIdx.x == 0) MX_TL(12, globaltimer());
   }
 
   if (warp == 0 || warp == 3) {
@@ -437,33 +518,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ok) {
     const uint32_t red_addr = smem_u32(red);
     __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(p.out);
-    for (int item = split + S * warp; item < p.M * 4; item += 4 * S) {
+    // Item = 32 columns of one row. A block nobody consumes (no bf16 output,
+    // outside the requantized and the summed-square columns) is not reduced: a peer's shared memory is
+    // read only for a value that is then used, so no read is in flight when the
+    // peers exit.
+    auto wanted = [&](int item) {
+      return item < p.M * 4 && (out != nullptr || (kRequant && tile * 128 + (item & 3) * 32 < p.q_cols) ||
+                                (p.ssq_out != nullptr && tile * 128 + (item & 3) * 32 < p.ssq_cols));
+    };
+    auto item_addr = [&](int item) {
+      return red_addr + static_cast<uint32_t>((item >> 2) * 128 + (item & 3) * 32 + lane) * 4u;
+    };
+    // bf16 store and MX requantization of one reduced item (warp-uniform call)
+    auto emit = [&](int item, float acc) {
       const int m = item >> 2;
-      const int nl = (item & 3) * 32 + lane;
-      const uint32_t off = red_addr + static_cast<uint32_t>(m * 128 + nl) * 4u;
-      const float acc = cluster_sum(off, S);
+      const int col = tile * 128 + (item & 3) * 32 + lane;
       const __nv_bfloat16 hb = __float2bfloat16_rn(acc);
-      const int col = tile * 128 + nl;
       if (out != nullptr) out[static_cast<size_t>(m) * p.N + col] = hb;
+      if (p.ssq_out != nullptr && tile * 128 + (item & 3) * 32 < p.ssq_cols) {
+        // the block's sum of squares: the xor-shuffle tree over its 32 values
+        const float v = __bfloat162float(hb);
+        float sq = __fmul_rn(v, v);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xFFFFFFFFu, sq, o));
+        if (lane == 0) p.ssq_out[static_cast<size_t>(m) * (p.ssq_cols >> 5) + (col >> 5)] = sq;
+      }
       if (kRequant && tile * 128 + (item & 3) * 32 < p.q_cols) {
         const float v = __bfloat162float(hb);
-        float amax = fabsf(v);
-        uint32_t nonfinite = !isfinite(v);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-          nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, o);
-        }
+        // block amax in one reduction: non-negative floats order as their
+        // bits, and an Inf or NaN puts the maximum at or above Inf's bits
+        const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v)));
         uint32_t sbyte, code;
-        if (nonfinite) {
+        if (amax_bits >= 0x7F800000u) {
           sbyte = 0xFFu;
           code = 0x7Fu;
         } else {
-          sbyte = mx_scale_byte(amax);
+          sbyte = mx_scale_byte(__uint_as_float(amax_bits));
           code = cvt_e4m3x2(v * mx_inv_scale(sbyte), 0.f) & 0xFFu;
         }
         p.q[static_cast<size_t>(m) * p.q_cols + col] = static_cast<uint8_t>(code);
         if (lane == 0) p.q_scales[swz_offset(m, col >> 5, p.q_cols >> 5)] = static_cast<uint8_t>(sbyte);
+      }
+    };
+    if (p.M <= S) {
+      // at most one item per warp
+      for (int item = split + S * warp; item < p.M * 4; item += 4 * S)
+        if (wanted(item)) emit(item, cluster_sum(item_addr(item), S));
+    } else {
+      // several items per warp: four items' peer loads in flight at once (the
+      // warp is alone on its scheduler, so one item at a time would be
+      // latency-bound), each still summed in rank order
+      for (int i0 = split + S * warp; i0 < p.M * 4; i0 += 4 * S * kSumBatch) {
+        uint32_t offs[kSumBatch];
+        bool use[kSumBatch];
+        float sums[kSumBatch];
+#pragma unroll
+        for (int b = 0; b < kSumBatch; ++b) {
+          use[b] = wanted(i0 + b * 4 * S);
+          offs[b] = item_addr(i0 + b * 4 * S);
+        }
+        cluster_sum_batch(offs, use, S, sums);
+#pragma unroll
+        for (int b = 0; b < kSumBatch; ++b)
+          if (use[b]) emit(i0 + b * 4 * S, sums[b]);  // use[] is warp-uniform
       }
     }
     if (kRequant && split == 0 && tile * 128 < p.q_cols) {
@@ -528,56 +645,72 @@ static int table_splits(int M, int N, int K) {
   return 0;
 }
 
-GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a) {
-  GemmPlan pl{};
-  pl.mtile = (M + 15) & ~15;
+GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a, bool norm) {
+  const int mtile = (M + 15) & ~15;
   const int tiles = N / 128;
   const int nchunks = K / 128;
-  const int nsfb = (pl.mtile + 127) / 128;
-  int splits = std::max(1, sm_count / std::max(tiles, 1));
-  // the table was measured with 152 SMs; other parts keep the SM-count rule
-  if (sm_count == 152 && table_splits(M, N, K) > 0) splits = table_splits(M, N, K);
-  splits = std::min(splits, std::min(8, nchunks));
-  if (const char* e = getenv("MX_SPLITS")) {
-    const int v = atoi(e);
-    if (v >= 1 && v <= 16) splits = std::min(v, nchunks);
-  }
+  const int nsfb = (mtile + 127) / 128;
+  const int xrows = std::min(M, kRowBatch);
   // the scale tiles of a CTA's K-range stay resident: at most 48 KB of them
   auto scale_bytes = [&](int sp) {
     return static_cast<size_t>((nchunks + sp - 1) / sp) * kSfTileBytes * (1 + nsfb);
   };
-  while (splits < std::min(8, nchunks) && scale_bytes(splits) > 48 * 1024) ++splits;
-  pl.splits = splits;
-  const int per_cta = (nchunks + splits - 1) / splits;
-  const int xrows = std::min(M, kRowBatch);
-  const Layout L1(pl.mtile, 1, per_cta, fused_a, xrows);
-  // resident per CTA besides the ring: scale tiles (and, fused, the activation
-  // tiles and the bf16 staging rows)
-  const size_t scales = L1.bars - L1.ring_bytes;
-  // Short K-ranges (all chunks in flight at once): about 100 KB per CTA, so the
-  // next kernel's CTAs fit beside this one. Long ones: as deep a ring as lets
-  // the whole grid be resident in one wave (CTAs per SM x shared memory).
-  const int per_sm = (tiles * splits + sm_count - 1) / std::max(sm_count, 1);
-  const size_t wave = per_sm <= 1 ? 180 * 1024 : 227 * 1024 / static_cast<size_t>(per_sm) - 4 * 1024;
-  const size_t budget = per_cta <= 8 ? std::min<size_t>(100 * 1024, wave) : wave;
-  int stages = budget > scales ? static_cast<int>((budget - scales) / L1.stage_bytes) : 0;
-  stages = std::max(2, std::min(stages, 10));
-  if (const char* e = getenv("MX_STAGES")) {
+  // the plan for a given number of K splits
+  auto plan_for = [&](int splits) {
+    GemmPlan pl{};
+    pl.mtile = mtile;
+    while (splits < std::min(8, nchunks) && scale_bytes(splits) > 48 * 1024) ++splits;
+    pl.splits = splits;
+    const int per_cta = (nchunks + splits - 1) / splits;
+    const Layout L1(mtile, 1, per_cta, fused_a, xrows, norm ? K / 32 : 0);
+    // resident per CTA besides the ring: scale tiles (and, fused, the activation
+    // tiles and the bf16 staging rows)
+    const size_t scales = L1.bars - L1.ring_bytes;
+    // Short K-ranges (all chunks in flight at once): about 100 KB per CTA, so
+    // the next kernel's CTAs fit beside this one. Long ones: as deep a ring as
+    // lets the whole grid be resident in one wave (CTAs per SM x shared memory).
+    const int per_sm = (tiles * splits + sm_count - 1) / std::max(sm_count, 1);
+    const size_t wave = per_sm <= 1 ? 180 * 1024 : 227 * 1024 / static_cast<size_t>(per_sm) - 4 * 1024;
+    const size_t budget = per_cta <= 8 ? std::min<size_t>(100 * 1024, wave) : wave;
+    int stages = budget > scales ? static_cast<int>((budget - scales) / L1.stage_bytes) : 0;
+    stages = std::max(2, std::min(stages, 10));
+    if (const char* e = getenv("MX_STAGES")) {
+      const int v = atoi(e);
+      if (v >= 1 && v <= 12) stages = v;
+    }
+    stages = std::min(stages, per_cta);
+    // the epilogue stages the fp32 partials [mtile][128] over the ring and what follows it
+    while (static_cast<size_t>(stages) * L1.stage_bytes + scales < static_cast<size_t>(mtile) * 512)
+      ++stages;
+    pl.stages = stages;
+    pl.tmem_cols = pow2_at_least(tmem_sfa_col(mtile) + 4 * stages * (1 + nsfb));
+    const Layout L(mtile, stages, per_cta, fused_a, xrows, norm ? K / 32 : 0);
+    // CTAs that can share an SM must fit their TMEM together: ask for enough
+    // shared memory that at most 512 / tmem_cols of them are resident.
+    const int max_res = 512 / pl.tmem_cols;
+    const size_t min_smem = 233472 / static_cast<size_t>(max_res + 1) + 1;
+    pl.smem = std::max(L.total(), min_smem);
+    return pl;
+  };
+  int splits = std::max(1, sm_count / std::max(tiles, 1));
+  // the table was measured with 152 SMs; other parts keep the SM-count rule
+  if (sm_count == 152 && table_splits(M, N, K) > 0) splits = table_splits(M, N, K);
+  splits = std::min(splits, std::min(8, nchunks));
+  bool forced = false;
+  if (const char* e = getenv("MX_SPLITS")) {
     const int v = atoi(e);
-    if (v >= 1 && v <= 12) stages = v;
+    if (v >= 1 && v <= 16) {
+      splits = std::min(v, nchunks);
+      forced = true;
+    }
   }
-  stages = std::min(stages, per_cta);
-  // the epilogue stages the fp32 partials [mtile][128] over the ring and what follows it
-  while (static_cast<size_t>(stages) * L1.stage_bytes + scales < static_cast<size_t>(pl.mtile) * 512)
-    ++stages;
-  pl.stages = stages;
-  pl.tmem_cols = pow2_at_least(tmem_sfa_col(pl.mtile) + 4 * stages * (1 + nsfb));
-  const Layout L(pl.mtile, stages, per_cta, fused_a, xrows);
-  // CTAs that can share an SM must fit their TMEM together: ask for enough
-  // shared memory that at most 512 / tmem_cols of them are resident.
-  const int max_res = 512 / pl.tmem_cols;
-  const size_t min_smem = 233472 / static_cast<size_t>(max_res + 1) + 1;
-  pl.smem = std::max(L.total(), min_smem);
+  GemmPlan pl = plan_for(splits);
+  // An accumulator of more than half the TMEM (mtile above ~230 rows) leaves
+  // room for one CTA per SM: a grid beyond one CTA per SM would run in two
+  // waves (M = 256, N = 5120, K = 8192: 240 CTAs, 36 us against 19 us at 192
+  // rows), so such plans take at most one CTA per SM.
+  if (!forced && pl.tmem_cols > 256 && tiles * pl.splits > sm_count)
+    pl = plan_for(std::max(1, std::min(pl.splits, sm_count / std::max(tiles, 1))));
   return pl;
 }
 

@@ -44,6 +44,23 @@ struct GemmPlan {
   size_t smem;
 };
 
+// RMS norm of the bf16 activation rows before their quantization (in-kernel
+// quantization only; gamma null = none): y = bf16(x * 1/sqrt(mean(x^2) + eps) *
+// gamma), the mean over the row's K values. The sum of squares is read, not
+// computed: ssq [M, K/32] holds each 32-block's sum of its squares (written by
+// the previous GEMM's epilogue, ssq_out), added here in block order. Tile 0's
+// CTAs also write, over their K-range, the normalized rows to y [M, K] and the
+// MXFP8 activation to a_q [M, K] and its swizzled scales a_q_scales (each null =
+// not written).
+struct GemmNorm {
+  const uint16_t* gamma;
+  float eps;
+  const float* ssq;
+  uint16_t* y;
+  uint8_t* a_q;
+  uint8_t* a_q_scales;
+};
+
 struct GemmArgs {
   int M, N, K;
   int mtile, stages, nchunks, tmem_cols;
@@ -53,6 +70,7 @@ struct GemmArgs {
   // kernel instead of MXFP8 activations through tm_a / a_scales; null = MXFP8 in
   const uint16_t* x;
   long ldx;
+  GemmNorm norm;
   // Grouped activations (0 = not grouped): weight tile t belongs to group
   // g = t / group_tiles and contracts the group's K-slice [g K, (g + 1) K) of
   // a wider MXFP8 activation whose scale layout has a_sf_chunks 128-wide
@@ -63,6 +81,11 @@ struct GemmArgs {
   uint8_t* q;         // fused requantization of columns [0, q_cols): E4M3 [M, q_cols]
   uint8_t* q_scales;  // swizzled scales of q
   int q_cols;
+  // per-32-block sums of squares of the bf16 output, columns [0, ssq_cols):
+  // ssq_out[m * ssq_cols / 32 + c / 32], each the xor-shuffle tree over the
+  // block's 32 values (null = not written)
+  float* ssq_out;
+  int ssq_cols;
   int* status;
 #ifdef MX_TIMELINE
   unsigned long long* tl;  // kTimelineSlots %globaltimer stamps per CTA, or null
@@ -71,14 +94,65 @@ struct GemmArgs {
 
 #ifdef MX_TIMELINE
 // Timeline build only: stamps per CTA of one GEMM launch (see gemm.cu).
-constexpr int kTimelineSlots = 12;
+constexpr int kTimelineSlots = 16;
 constexpr int kTimelineCtas = 512;
 #endif
 
-GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a = false);
+// fused_a: bf16 activations quantized in the kernel; norm: with the RMS norm.
+GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a = false, bool norm = false);
 cudaError_t set_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& args,
                         const GemmPlan& plan, bool pdl, cudaStream_t stream);
+
+// ------------------------------------------------------------ persistent chain
+// The three projections of mx_gemm_chain in one persistent kernel (chain.cu):
+// clusters of kChainCluster CTAs, one CTA per SM, every CTA resident at once.
+constexpr int kChainCluster = 8;
+constexpr int kChainMaxUnits = 8;      // (tile, K split) work units per CTA, all projections
+constexpr int kChainCounters = 16384;  // 32-bit words of the handle's chain workspace
+
+// One projection as the chain kernel sees it.
+struct ChainProj {
+  const uint8_t* w_scales;  // swizzled [n, k/32]
+  const uint8_t* a_scales;  // swizzled scales of the activation [M, k]
+  int n, k;
+  int splits;               // CTAs (ranks of one cluster) sharing a weight tile's K-range
+  void* out;                // bf16 [M, n], or null
+  uint8_t* q;               // MX requantization of columns [0, q_cols): the next activation
+  uint8_t* q_scales;
+  int q_cols;
+};
+
+// Shared-memory and TMEM plan of the chain kernel (offsets from the CTA's
+// 1024-aligned base); ok == false: the three-launch path serves the call.
+struct ChainPlan {
+  bool ok;
+  int clusters, ring, tmem_cols;
+  int act_chunks[3], max_units[3];
+  uint32_t off_act[3], off_asf[3], off_staged, off_recv[3], recv_unit_bytes[3], off_bars;
+  size_t smem;
+};
+
+struct ChainArgs {
+  int M, mtile, nsfb;
+  ChainProj proj[3];
+  ChainPlan plan;
+  // workspace: [0] calls completed, [1] CTAs finished in this call, [2] abort,
+  // then one counter per weight tile of the first two projections (from
+  // cnt_off), zero at the start of every call
+  unsigned* counters;
+  int cnt_off[2];
+  int* status;
+#ifdef MX_TIMELINE
+  unsigned long long* tl;  // kTimelineSlots %globaltimer stamps per CTA, or null
+#endif
+};
+
+ChainPlan plan_chain(int M, const ChainProj (&proj)[3], int clusters);
+// Clusters of kChainCluster CTAs of the chain kernel that can be resident at once.
+int chain_max_clusters();
+cudaError_t set_chain_attributes();
+cudaError_t launch_chain(const CUtensorMap (&maps)[6], const ChainArgs& args, cudaStream_t stream);
 
 // ------------------------------------------------------------ grouped WO-A
 struct WoaPlan {

@@ -12,6 +12,10 @@ constexpr int kStatusTimeout = 1;   // a bounded wait expired
 constexpr int kStatusBadInput = 2;  // device-side data out of range (e.g. a position)
 // Upper bound of any single wait on an mbarrier, in nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Bound of a wait for data a peer CTA sends at the end of its own pipeline: a
+// peer reaches its send even after its own bounded waits expired (a few of
+// them at most), so this bound outlasts any peer's way there.
+constexpr uint64_t kPeerWaitLimitNs = 8 * kWaitLimitNs;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -45,13 +49,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase of the given parity to complete; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((i & 255u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
 }
 
@@ -98,6 +103,22 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's earlier generic-proxy accesses of global memory (e.g. an
+// acquire of data another CTA wrote) before its later async-proxy ones (TMA).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ------------------------------------------------------ global synchronization
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Barrier among `threads` threads (whole warps) of the CTA on hardware barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // ------------------------------------------------------------------ cluster
 __device__ __forceinline__ void cluster_sync() {
@@ -109,6 +130,30 @@ __device__ __forceinline__ void cluster_sync() {
 // release barrier would also wait for this thread's global stores to complete.
 __device__ __forceinline__ void cluster_sync_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+// The two halves of a cluster barrier, for a phase whose arrival and wait are
+// far apart (arrive at set-up, wait just before the first access to a peer).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Bulk copy from this CTA's shared memory into a peer's (dst and the peer's
+// mbarrier from mapa), counted on that barrier (complete_tx); 16-byte aligned,
+// bytes % 16 == 0. Committed to this thread's bulk async-group.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the source reads of this thread's committed bulk copies are done.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -137,6 +182,31 @@ __device__ __forceinline__ float cluster_sum(uint32_t addr, int S) {
       if (r0 + r < S) acc += v[r];
   }
   return acc;
+}
+
+// cluster_sum for kSumBatch addresses at once: every (address, rank) load of a
+// group of 8 ranks is issued before any add, so the items' latencies overlap;
+// each sum is still taken in rank order (the same result as cluster_sum).
+// Addresses with use[b] == false are not read and sum to 0.
+constexpr int kSumBatch = 4;
+__device__ __forceinline__ void cluster_sum_batch(const uint32_t (&addr)[kSumBatch],
+                                                  const bool (&use)[kSumBatch], int S,
+                                                  float (&sum)[kSumBatch]) {
+#pragma unroll
+  for (int b = 0; b < kSumBatch; ++b) sum[b] = 0.f;
+  for (int r0 = 0; r0 < S; r0 += 8) {
+    float v[kSumBatch][8];
+#pragma unroll
+    for (int b = 0; b < kSumBatch; ++b)
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        v[b][r] = use[b] && r0 + r < S ? ld_shared_cluster_f32(map_shared_rank(addr[b], r0 + r)) : 0.f;
+#pragma unroll
+    for (int b = 0; b < kSumBatch; ++b)
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r0 + r < S) sum[b] += v[b][r];
+  }
 }
 
 // ------------------------------------------------------------------ warp
@@ -231,6 +301,21 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_lh(uint32_t taddr, uint32_t l
                "tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], d;\n\t}" ::"r"(taddr),
                "r"(lo), "r"(hi)
                : "memory");
+}
+// Each thread of the warp reads 16 consecutive 32-bit columns of its TMEM lane,
+// without waiting (tmem_ld_wait makes the registers valid).
+__device__ __forceinline__ void tmem_ld_32x32b_x16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 // Each thread of the warp reads 16 consecutive 32-bit columns of its TMEM lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&v)[16]) {

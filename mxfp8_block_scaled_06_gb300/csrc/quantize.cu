@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
 // RMS normalization + MX quantization of rows (the split between the first two
 // decode projections): one warp per row; pass 1 sums the squares of the row in
-// float32 (each lane over its units in order, then xor-shuffles: a fixed order),
+// float32 in a fixed order (per 32-block a tree, then the blocks in order),
 // pass 2 scales each element by 1/sqrt(mean + eps) (correctly rounded sqrt and
 // division) and the row's weight, rounds to bf16 (optionally stored) and
 // quantizes per 32-block as quantize_rows_kernel does.
@@ -137,23 +137,41 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int groups = (cpad4 + 7) / 8;  // 8 blocks (256 elements) per pass of the warp
   const bool real = row < M;
   const uint16_t* const xr = x + static_cast<size_t>(row) * ldx;
+  // Sum of squares: each 32-block's squares are added in the xor-shuffle tree
+  // over the block's 32 elements (element j pairs with j ^ 16, then j ^ 8, ...:
+  // the order the GEMM epilogue uses when it writes a row's block sums), and the
+  // block sums in block order. Lane l holds elements 8 (l & 3) .. 8 (l & 3) + 7 of
+  // block l / 4: the tree's first two levels pair lanes (l ^ 2, l ^ 1), the last
+  // three pair elements within the lane.
   float ss = 0.f;
-  if (real) {
-    for (int g = 0; g < groups; ++g) {
-      const int blk = g * 8 + (lane >> 2);
-      if (blk >= nblk) continue;
-      const uint4 raw = *reinterpret_cast<const uint4*>(xr + blk * 32 + (lane & 3) * 8);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  for (int g = 0; g < groups; ++g) {
+    const int blk = g * 8 + (lane >> 2);
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (real && blk < nblk) raw = *reinterpret_cast<const uint4*>(xr + blk * 32 + (lane & 3) * 8);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float s[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
-        ss = __fadd_rn(ss, __fmul_rn(a, a));
-        ss = __fadd_rn(ss, __fmul_rn(b, b));
-      }
+    for (int i = 0; i < 4; ++i) {
+      const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
+      s[2 * i] = __fmul_rn(a, a);
+      s[2 * i + 1] = __fmul_rn(b, b);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] = __fadd_rn(s[e], __shfl_xor_sync(0xFFFFFFFFu, s[e], 2));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] = __fadd_rn(s[e], __shfl_xor_sync(0xFFFFFFFFu, s[e], 1));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] = __fadd_rn(s[e], s[e + 4]);
+    s[0] = __fadd_rn(s[0], s[2]);
+    s[1] = __fadd_rn(s[1], s[3]);
+    s[0] = __fadd_rn(s[0], s[1]);
+    // block g * 8 + b sits in lanes 4b .. 4b + 3; every lane adds the same sequence
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const float blk_sum = __shfl_sync(0xFFFFFFFFu, s[0], 4 * b);
+      if (g * 8 + b < nblk) ss = __fadd_rn(ss, blk_sum);
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
   const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps)));
   for (int g = 0; g < groups; ++g) {
     const int blk = g * 8 + (lane >> 2);

@@ -360,33 +360,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t red_addr = smem_u32(red);
     const int qcols = p.G * p.R;
     const int nwarps = kThreads / 32;
-    for (int item = split + S * warp; item < p.T * 4; item += nwarps * S) {
-      const int m = item >> 2;
-      const int nl = (item & 3) * 32 + lane;
-      const uint32_t off = red_addr + static_cast<uint32_t>(m * 128 + nl) * 4u;
-      const float acc = cluster_sum(off, S);
-      const __nv_bfloat16 hb = __float2bfloat16_rn(acc);
-      const int col = g * p.R + rt * 128 + nl;
-      if (p.debug_z)
-        p.debug_z[static_cast<size_t>(m) * qcols + col] = __bfloat16_as_ushort(hb);
-      const float v = __bfloat162float(hb);
-      float amax = fabsf(v);
-      uint32_t nonfinite = !isfinite(v);
+    // four items' peer loads in flight at once, each summed in rank order
+    for (int i0 = split + S * warp; i0 < p.T * 4; i0 += nwarps * S * kSumBatch) {
+      uint32_t offs[kSumBatch];
+      bool use[kSumBatch];
+      float sums[kSumBatch];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, o);
+      for (int b = 0; b < kSumBatch; ++b) {
+        const int item = i0 + b * nwarps * S;
+        use[b] = item < p.T * 4;
+        offs[b] = red_addr + static_cast<uint32_t>((item >> 2) * 128 + (item & 3) * 32 + lane) * 4u;
       }
-      uint32_t sbyte, code;
-      if (nonfinite) {
-        sbyte = 0xFFu;
-        code = 0x7Fu;
-      } else {
-        sbyte = mx_scale_byte(amax);
-        code = cvt_e4m3x2(v * mx_inv_scale(sbyte), 0.f) & 0xFFu;
+      cluster_sum_batch(offs, use, S, sums);
+#pragma unroll
+      for (int b = 0; b < kSumBatch; ++b) {
+        if (!use[b]) continue;  // warp-uniform
+        const int item = i0 + b * nwarps * S;
+        const int m = item >> 2;
+        const int col = g * p.R + rt * 128 + (item & 3) * 32 + lane;
+        const __nv_bfloat16 hb = __float2bfloat16_rn(sums[b]);
+        if (p.debug_z)
+          p.debug_z[static_cast<size_t>(m) * qcols + col] = __bfloat16_as_ushort(hb);
+        const float v = __bfloat162float(hb);
+        // block amax in one reduction: non-negative floats order as their
+        // bits, and an Inf or NaN puts the maximum at or above Inf's bits
+        const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v)));
+        uint32_t sbyte, code;
+        if (amax_bits >= 0x7F800000u) {
+          sbyte = 0xFFu;
+          code = 0x7Fu;
+        } else {
+          sbyte = mx_scale_byte(__uint_as_float(amax_bits));
+          code = cvt_e4m3x2(v * mx_inv_scale(sbyte), 0.f) & 0xFFu;
+        }
+        p.q[static_cast<size_t>(m) * qcols + col] = static_cast<uint8_t>(code);
+        if (lane == 0) p.q_scales[swz_offset(m, col >> 5, qcols >> 5)] = static_cast<uint8_t>(sbyte);
       }
-      p.q[static_cast<size_t>(m) * qcols + col] = static_cast<uint8_t>(code);
-      if (lane == 0) p.q_scales[swz_offset(m, col >> 5, qcols >> 5)] = static_cast<uint8_t>(sbyte);
     }
     if (split == 0) {
       const int mpad = (p.T + 127) & ~127;

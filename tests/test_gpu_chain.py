@@ -125,3 +125,18 @@ def _vs_oracle(m, shapes, g1_cols, seed):
         tol = oracle.gemm_tolerance(ref) + extra
         bad = ~(np.abs(got - ref) <= tol)
         assert not bad.any(), f"stage {stage + 2}: {int(bad.sum())} elements beyond tolerance"
+
+
+@pytest.mark.parametrize("m", [1, 16, 64])
+def test_chain_without_debug_outputs(m):
+    """Without the debug copies of out1 / out2 - G1's columns past g1_cols then
+    feed nothing - the chain writes the same a2, a3 and out as with them."""
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    shapes = [(2048, 5120), (8192, 1536), (5120, 8192)]
+    ws, (aq, asc), _, res = _run_chain(m, shapes, 1536, seed=2)
+    res2 = mx.mx_gemm_chain(handle(), aq, asc, [w[0] for w in ws], g1_cols=1536)
+    torch.cuda.synchronize()
+    assert mx.mx_device_status(handle()) == mx.MX_OK
+    for name in ("a2", "a2_scales", "a3", "a3_scales", "out"):
+        assert torch.equal(res2[name].view(torch.uint8), res[name].view(torch.uint8)), name

@@ -7,9 +7,12 @@
   oracle's codes on every 32-block whose y agrees;
 * closed forms: a constant row with weight 1 and eps 0 normalizes to exactly
   +-1; a zero row with eps > 0 stays zero (scale byte 0);
-* the chain with the norm equals composing the entry points on the GPU, bit for
-  bit, and its output stays within the GEMM tolerance of the oracle's GEMM on
-  the GPU's own last activation.
+* the chain with the norm equals composing the entry points on the GPU
+  (mx_gemm, mx_rmsnorm_quantize_rows, mx_gemm, mx_quantize_rows, mx_gemm), bit
+  for bit, in both of its forms (up to 16 rows the norm and quantization run
+  in G2's prologue; above, the norm kernel runs between G1 and G2), and its
+  output stays within the GEMM tolerance of the oracle's GEMM on the GPU's own
+  last activation.
 """
 import numpy as np
 import pytest
@@ -126,21 +129,20 @@ def _dequant_torch(codes: np.ndarray, plain_scales: np.ndarray) -> np.ndarray:
     return (v.reshape(m, k // 32, 32) * sc[..., None]).reshape(m, k).numpy()
 
 
-@pytest.mark.parametrize("m", [1, 8, 40])
-def test_chain_norm_equals_composition_and_oracle(m):
+def _chain_norm_composition(m, shapes, g1_cols, seed):
+    """mx_gemm_chain_norm against the composition of the entry points, bit for bit."""
     import mxfp8_block_scaled_06_gb300 as mx
 
-    shapes = [(2048, 5120), (8192, 1536), (5120, 8192)]
-    wops = [operands(60 + i, synth.TAG_W + i, n, k) for i, (n, k) in enumerate(shapes)]
+    wops = [operands(seed + i, synth.TAG_W + i, n, k) for i, (n, k) in enumerate(shapes)]
     ws = [quantize_on_gpu(bits) for bits, _, _ in wops]
-    a_bits, _, (ra, rsa) = operands(61, synth.TAG_A, m, 5120, -4, 4)
+    a_bits, _, (ra, rsa) = operands(seed + 1, synth.TAG_A, m, shapes[0][1], -4, 4)
     aq, asc = quantize_on_gpu(a_bits)
-    nw_bits = _weight(1536, 62)
+    nw_bits = _weight(g1_cols, seed + 2)
     nw = bf16_to_device(nw_bits)
     h = handle()
-    res = mx.mx_gemm_chain_norm(h, aq, asc, ws, nw, 1e-6, debug=True)
+    res = mx.mx_gemm_chain_norm(h, aq, asc, ws, nw, 1e-6, g1_cols=g1_cols, debug=True)
     o1 = mx.mx_gemm(h, aq, asc, *ws[0])
-    a2, a2s, y = mx.mx_rmsnorm_quantize_rows(h, o1[:, :1536], nw, 1e-6, y=True)
+    a2, a2s, y = mx.mx_rmsnorm_quantize_rows(h, o1[:, :g1_cols], nw, 1e-6, y=True)
     o2 = mx.mx_gemm(h, a2, a2s, *ws[1])
     a3, a3s = mx.mx_quantize_rows(h, o2)
     o3 = mx.mx_gemm(h, a3, a3s, *ws[2])
@@ -152,6 +154,19 @@ def test_chain_norm_equals_composition_and_oracle(m):
                             ("a3", res["a3"], a3), ("a3_scales", res["a3_scales"], a3s),
                             ("out", res["out"], o3)]:
         assert torch.equal(got.view(torch.uint8), want.view(torch.uint8)), name
+    return res, wops, ra, rsa, nw_bits
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_chain_norm_small_shapes(m):
+    # a shorter normalized row (g1_cols = 256: 8 blocks, fewer than a lane's loads)
+    _chain_norm_composition(m, [(384, 640), (256, 256), (512, 256)], 256, seed=70)
+
+
+@pytest.mark.parametrize("m", [1, 5, 16, 17, 40, 130])
+def test_chain_norm_equals_composition_and_oracle(m):
+    shapes = [(2048, 5120), (8192, 1536), (5120, 8192)]
+    res, wops, ra, rsa, nw_bits = _chain_norm_composition(m, shapes, 1536, seed=60)
     # 2. against the oracle chain on the oracle's own operands
     ora = oracle.chain_norm(ra, rsa, [ops[2] for ops in wops], synth.bf16_bits_to_f64(nw_bits), 1e-6)
     assert_gemm_close(res["out1"], ora["out1"], "chain-norm G1")

@@ -7,7 +7,10 @@
 * q / q_scales equal mx_quantize_rows of the GPU's own bf16 z, bit for bit,
   and agree with the oracle's on every 32-block whose bf16 z agrees;
 * the wo_b GEMM on q (K = 4096, N = 5120) stays within the GEMM tolerance plus
-  the exact effect of the few codes that differ.
+  the exact effect of the few codes that differ;
+* called without the debug copy of the activation above 8 tokens, the call
+  takes the two launches on the handle's scratch: the same checks, plus bit
+  equality with wo_a_grouped_unfused, also for calls of shrinking sizes in a row.
 """
 import numpy as np
 import pytest
@@ -107,6 +110,54 @@ def test_wo_a_then_wo_b():
     extra = 1.01 * (delta @ np.abs(oracle.mx_dequantize(rb, rbs)).T)
     got = out.float().cpu().numpy().astype(np.float64)
     assert (np.abs(got - ref) <= oracle.gemm_tolerance(ref) + extra).all()
+
+
+FUSED_MAX_TOKENS = 8  # wo_a_grouped's documented switch to the two launches
+
+
+def _without_debug_copy(t, seed=3):
+    """wo_a_grouped asked for z only (no debug copy of the activation): above 8
+    tokens it runs the two launches on the handle's scratch. Checked against the
+    oracle like the fused kernel, and there bit for bit against
+    wo_a_grouped_unfused on caller buffers."""
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    (wq, wsc), (rw, rws), cs, cs_dev = _setup()
+    x_bits = synth.normal_bf16(seed + t, synth.TAG_X, (t, G * H, D))
+    pos = synth.positions(seed + t, synth.TAG_POS, t)
+    x = bf16_to_device(x_bits)
+    pos_dev = torch.from_numpy(pos).cuda()
+    res = mx.wo_a_grouped(handle(), x, pos_dev, cs_dev, wq, wsc, G, H, R, z=True, early_trigger=True)
+    torch.cuda.synchronize()
+    assert mx.mx_device_status(handle()) == mx.MX_OK
+    assert res["xq"] is None and res["xs"] is None
+    if t > FUSED_MAX_TOKENS:
+        ref = mx.wo_a_grouped_unfused(handle(), x, pos_dev, cs_dev, wq, wsc, G, H, R, z=True)
+        torch.cuda.synchronize()
+        assert torch.equal(res["z"], ref["z"])
+        assert torch.equal(res["q"], ref["q"]) and torch.equal(res["q_scales"], ref["q_scales"])
+    ora = oracle.wo_a_grouped(synth.bf16_bits_to_f64(x_bits), pos, cs, rw, rws, G, H, 448, 64, R)
+    assert_gemm_close(res["z"], ora["z"], "WO-A z (two launches)")
+    q2, s2 = mx.mx_quantize_rows(handle(), res["z"])
+    torch.cuda.synchronize()
+    assert torch.equal(res["q"], q2) and torch.equal(res["q_scales"], s2)
+    zb_gpu = res["z"].view(torch.int16).cpu().numpy().view(np.uint16)
+    same_block = (zb_gpu.reshape(t, -1, 32) == oracle.bf16_bits(ora["zb"]).reshape(t, -1, 32)).all(-1)
+    gq = u8(res["q"]).reshape(t, -1, 32)
+    assert (gq[same_block] == ora["q"].reshape(t, -1, 32)[same_block]).all()
+    assert same_block.mean() >= 0.95
+
+
+@pytest.mark.parametrize("t", [8, 9, 17, 32, 100, 128])
+def test_wo_a_without_debug_copy(t):
+    _without_debug_copy(t)
+
+
+def test_wo_a_two_launch_scratch_reused_across_calls():
+    # the handle's scratch keeps the previous call's activation: a smaller call
+    # after a larger one must not read any of it
+    for t in (128, 24, 64, 9):
+        _without_debug_copy(t, seed=9)
 
 
 def test_wo_a_rejects_unsupported_shapes():

@@ -74,3 +74,19 @@ def test_single_process_needs_no_process_group(monkeypatch):
     rep.barrier()
     assert rep.max_over_ranks(3.5) == 3.5
     assert rep.job_value(1.0e9, 1.0) == pytest.approx(1000.0)
+
+
+def test_gpus_flag_launches_its_own_replicas():
+    """bench.py --gpus 2 without torchrun starts two processes itself (ranks 0 and
+    1 over gloo on 127.0.0.1); only rank 0 prints, with n_gpus = 2."""
+    import subprocess
+
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--replica-selftest"],
+                       capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line == {"n_gpus": 2, "max_over_ranks": 2.0}

@@ -737,7 +737,7 @@ def run_timeline(args):
     out["step"] = record(step, 3)
     cset = rig.copies(sum(w_bytes(n, k) for n, k in CHAIN_SHAPES))
     cw = rig.weight_set(CHAIN_SHAPES, seed=2, ncopies=cset)
-    for m in (1, 16, 64):
+    for m in (1, 4, 16, 64):
         q1 = mx.mx_quantize_rows(h, rig.activation(m, CHAIN_SHAPES[0][1], seed=2, umin=-4, umax=4))
         bufs = dict(out=torch.empty((m, CHAIN_SHAPES[2][0]), dtype=torch.bfloat16, device=rig.dev),
                     a2=torch.empty((m, CHAIN_G1_COLS), dtype=torch.uint8, device=rig.dev),
@@ -758,6 +758,80 @@ def run_timeline(args):
     torch.cuda.synchronize()
     assert mx.mx_device_status(h) == mx.MX_OK
     print(json.dumps({"timeline": out}))
+
+
+TUNE_M = (1, 2, 4, 8, 16, 32, 48, 64)
+
+
+def run_tune_chain(args):
+    """--tune-chain: the K-split count and ring depth of each chain projection,
+    timed inside the graph-replayed mx_gemm_chain (not as isolated launches).
+    Per row count, greedily G1, then G2, then G3: each candidate (splits in
+    1..8, ring depth as planned or every chunk of the K-range resident) is set
+    for that projection alone through MX_PLAN_AT (on a handle created for the
+    candidate: overrides are read at mx_create), the projections already
+    chosen keep their pick, the rest their current plan; weights rotate over
+    >= 3x L2; each time is the median of 10 replays of 20 chained calls."""
+    import torch
+
+    import mxfp8_block_scaled_06_gb300 as mx
+    from mxfp8_block_scaled_06_gb300 import build as mxbuild
+
+    mxbuild.build()
+    torch.cuda.set_device(0)
+    h = mx.mx_create(0)
+    props = torch.cuda.get_device_properties(0)
+    rig = Rig(torch, mx, h, getattr(props, "L2_cache_size", 126 * 2**20))
+    stream = torch.cuda.Stream()
+    cset = rig.copies(sum(w_bytes(n, k) for n, k in CHAIN_SHAPES))
+    cw = rig.weight_set(CHAIN_SHAPES, seed=2, ncopies=cset)
+    spec = lambda picks: ",".join(f"{n}x{k}:{s}" + (f":{st}" if st else "")
+                                  for (n, k), (s, st) in picks.items())
+    out = {}
+    for m in TUNE_M:
+        q1 = mx.mx_quantize_rows(h, rig.activation(m, CHAIN_SHAPES[0][1], seed=2, umin=-4, umax=4))
+        bufs = dict(out=torch.empty((m, CHAIN_SHAPES[2][0]), dtype=torch.bfloat16, device=rig.dev),
+                    a2=torch.empty((m, CHAIN_G1_COLS), dtype=torch.uint8, device=rig.dev),
+                    a2_scales=torch.empty(mx.mx_scale_bytes(m, CHAIN_G1_COLS), dtype=torch.uint8,
+                                          device=rig.dev),
+                    a3=torch.empty((m, CHAIN_SHAPES[1][0]), dtype=torch.uint8, device=rig.dev),
+                    a3_scales=torch.empty(mx.mx_scale_bytes(m, CHAIN_SHAPES[1][0]), dtype=torch.uint8,
+                                          device=rig.dev))
+
+        def timed(plan_at, q1=q1, bufs=bufs):
+            # a handle reads the plan overrides once, when it is created
+            if plan_at:
+                os.environ["MX_PLAN_AT"] = plan_at
+            else:
+                os.environ.pop("MX_PLAN_AT", None)
+            hc = mx.mx_create(0)
+            os.environ.pop("MX_PLAN_AT", None)
+            try:
+                return median_us(torch, lambda i: mx.mx_gemm_chain(
+                    hc, q1[0], q1[1], cw[i % cset], g1_cols=CHAIN_G1_COLS, stream=stream, **bufs), 20, stream)
+            finally:
+                hc.close()
+
+        current = timed("")
+        picks, cands = {}, {}
+        for n, k in CHAIN_SHAPES:
+            times = {}
+            for s in range(1, min(8, k // 128) + 1):
+                for st in (0, 12):  # 0: ring depth as planned; 12: the whole K-range resident
+                    try:
+                        times[(s, st)] = timed(spec({**picks, (n, k): (s, st)}))
+                    except mx.MxError:  # no plan fits shared memory: the library rejects it
+                        pass
+            best = min(times, key=times.get)
+            picks[(n, k)] = best
+            cands[f"{n}x{k}"] = {f"s{s}" + ("_deep" if st else ""): round(t, 3) for (s, st), t in times.items()}
+        tuned = timed(spec(picks))
+        out[m] = {"current_us": round(current, 3), "tuned_us": round(tuned, 3), "MX_PLAN_AT": spec(picks),
+                  "candidates_us": cands}
+        print(json.dumps({m: out[m]}), file=sys.stderr, flush=True)
+    torch.cuda.synchronize()
+    assert mx.mx_device_status(h) == mx.MX_OK
+    print(json.dumps({"tune_chain": out}))
 
 
 def launch_replicas(n):
@@ -801,6 +875,8 @@ def main():
     ap.add_argument("--profile", default=None, choices=["gemm", "chain", "wo_a", "sweep"])
     ap.add_argument("--timeline", action="store_true",
                     help="per-CTA phase timeline of GEMM launches (builds the -DMX_TIMELINE library)")
+    ap.add_argument("--tune-chain", action="store_true",
+                    help="time each chain projection's K-split / ring-depth candidates inside the chain")
     ap.add_argument("--replica-selftest", action="store_true",
                     help="the replicas' host-side coordination only (no GPU), e.g. with --gpus 2")
     args = ap.parse_args()
@@ -811,6 +887,9 @@ def main():
         return
     if args.timeline:
         run_timeline(args)
+        return
+    if args.tune_chain:
+        run_tune_chain(args)
         return
     if args.profile:
         run_profile(args)

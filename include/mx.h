@@ -286,6 +286,34 @@ int wo_a_grouped_unfused(mx_handle* h, int T, const void* x, long ldx,
                          int d_rope, int R, void* xq, void* xq_scales, void* z, void* q,
                          void* q_scales, void* stream);
 
+/* Bytes of device scratch mx_warmup needs for these weights and row counts:
+ * round256(the largest rows*k) for the zero activation's codes, then
+ * round256(the largest mx_scale_bytes(rows, k)) for its scales, then one
+ * round256(rows*n*2)-byte bf16 output per (shape, row count) run, in the order
+ * of mx_warmup. 0 for invalid arguments (no weight or row count, rows < 1,
+ * k not a multiple of 32). Host-only: touches no device. */
+size_t mx_warmup_bytes(const mx_weight* w, int nw, const int* rows, int nrows);
+
+/* Readies the kernels for the weight shapes a model will run, before its first
+ * real call (the mxfp8 page's `compile_pinned`, `run_zeros` and `_zeros` over
+ * `shape_representatives`): for each distinct (n, k) among w[0..nw), in
+ * increasing (n, k) order, using the first weight of that shape, and for each
+ * row count rows[0..nrows) in the given order, computes and keeps the handle's
+ * GEMM plan, encodes the tensor maps and runs mx_gemm once on a zero MXFP8
+ * activation (zero codes, zero scale bytes), with PDL, on stream.
+ *   scratch  device buffer of at least mx_warmup_bytes(...) bytes, 256-byte
+ *            aligned: the call zeroes the activation part and writes each
+ *            run's [rows, n] bf16 output after it, in the layout
+ *            mx_warmup_bytes describes. With finite weights every output is 0.
+ * Every run is validated and prepared before the first launch: an invalid
+ * weight or row count (as mx_gemm would reject it: rows > 256, n % 128 or
+ * k % 128 != 0, a misaligned pointer) returns its error with nothing enqueued.
+ * Call it after mx_create and before any stream capture. The paper's
+ * counterpart compiles kernels; this library's kernels are loaded at mx_create,
+ * so what it readies are the plans, the tensor maps and the first launch. */
+int mx_warmup(mx_handle* h, const mx_weight* w, int nw, const int* rows, int nrows,
+              void* scratch, size_t scratch_bytes, void* stream);
+
 /* Read and clear the device status word: MX_OK, or MX_ERR_TIMEOUT if a kernel
  * gave up on a bounded wait since the last call. Synchronizes the device. */
 int mx_device_status(mx_handle* h, int* status);

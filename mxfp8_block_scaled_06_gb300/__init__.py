@@ -24,8 +24,8 @@ MX_FLAG_PDL = 1
 
 EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows",
            "mx_rmsnorm_quantize_rows", "mx_gemm", "mx_gemm_bf16", "mx_gemm_chain",
-           "mx_gemm_chain_norm", "mx_gemm_chain_noalloc", "wo_a_grouped", "wo_a_grouped_unfused", "mx_device_status",
-           "mx_wait_selftest", "mx_status_string"]
+           "mx_gemm_chain_norm", "mx_gemm_chain_noalloc", "wo_a_grouped", "wo_a_grouped_unfused",
+           "mx_warmup_bytes", "mx_warmup", "mx_device_status", "mx_wait_selftest", "mx_status_string"]
 
 _vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
 
@@ -65,6 +65,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx_gemm_chain.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp]
     lib.mx_gemm_chain_noalloc.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp]
+    lib.mx_warmup_bytes.argtypes = [ctypes.POINTER(MxWeight), _i, ctypes.POINTER(_i), _i]
+    lib.mx_warmup_bytes.restype = ctypes.c_size_t
+    lib.mx_warmup.argtypes = [_vp, ctypes.POINTER(MxWeight), _i, ctypes.POINTER(_i), _i, _vp,
+                              ctypes.c_size_t, _vp]
     lib.wo_a_grouped.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i,
                                  _vp, _vp, _vp, _vp, _vp, _i, _vp]
     lib.wo_a_grouped_unfused.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i,
@@ -467,6 +471,39 @@ def wo_a_grouped_unfused(h: Handle, x, positions, cos_sin, w, w_scales, n_groups
                                                _ptr(zt), _ptr(q), _ptr(q_scales), _stream(stream)),
            "wo_a_grouped_unfused")
     return dict(q=q, q_scales=q_scales, z=zt, xq=xq, xq_scales=xq_scales)
+
+
+def mx_warmup(h: Handle, weights, rows, stream=None) -> list:
+    """Ready the GEMM of every distinct weight shape at each row count (plans,
+    tensor maps, one launch on a zero MXFP8 activation). weights: (w, w_scales)
+    pairs; returns the runs' bf16 outputs ([rows, n], all zero for finite
+    weights) in run order: shapes in increasing (n, k), then rows as given."""
+    import torch
+    if not weights or not rows:
+        raise ValueError("mx_warmup needs at least one weight and one row count")
+    ws = (MxWeight * len(weights))(*[MxWeight(_ptr(w), _ptr(s), w.shape[0], w.shape[1])
+                                     for w, s in weights])
+    rr = (_i * len(rows))(*[int(r) for r in rows])
+    lib = load_library()
+    nbytes = int(lib.mx_warmup_bytes(ws, len(weights), rr, len(rows)))
+    if nbytes == 0:
+        raise MxError(MX_ERR_INVALID_ARG, "mx_warmup_bytes")
+    dev = weights[0][0].device
+    scratch = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+    off0 = (-scratch.data_ptr()) % 256
+    buf = scratch[off0:off0 + nbytes]
+    _check(lib.mx_warmup(h.ptr, ws, len(weights), rr, len(rows), _ptr(buf), nbytes, _stream(stream)),
+           "mx_warmup")
+    shapes = sorted({(w.shape[0], w.shape[1]) for w, _ in weights})
+    r256 = lambda v: (v + 255) // 256 * 256
+    off = r256(max(r * k for _, k in shapes for r in rows)) + \
+        r256(max(mx_scale_bytes(r, k) for _, k in shapes for r in rows))
+    outs = []
+    for n, k in shapes:
+        for r in rows:
+            outs.append(buf[off:off + r * n * 2].view(torch.bfloat16).view(r, n))
+            off += r256(r * n * 2)
+    return outs
 
 
 def mx_device_status(h: Handle) -> int:

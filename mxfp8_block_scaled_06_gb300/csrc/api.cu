@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "../../include/mx.h"
 #include "kernels.h"
@@ -24,9 +25,22 @@ struct TmapEntry {
 };
 constexpr int kTmapCache = 32;
 
+// GEMM plans the handle has computed, by problem.
+struct PlanEntry {
+  int M, N, K;
+  bool fused, norm;
+  mx::GemmPlan plan;
+};
+constexpr int kPlanCache = 64;
+
 struct mx_handle {
   int device;
   int sm_count;
+  mx::PlanEnv env;        // plan overrides, read once at mx_create
+  bool chain_persistent;  // MX_CHAIN_PERSISTENT=1 at mx_create
+  PlanEntry plans[kPlanCache];
+  int plan_count;
+  int plan_next;  // round-robin replacement
   int* d_status;
   unsigned* d_chain;   // persistent chain kernel's counters (kChainCounters words)
   int chain_clusters;  // clusters of 8 CTAs it may use (0: the three-launch path only)
@@ -66,6 +80,8 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
 int check_device(const mx_handle* h) {
   if (h == nullptr) return MX_ERR_INVALID_ARG;
   int cur = -1;
@@ -74,6 +90,20 @@ int check_device(const mx_handle* h) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+// The GEMM plan of a problem, computed once per handle (mx_warmup computes those
+// of the registered shapes ahead of the first call).
+mx::GemmPlan get_plan(mx_handle* h, int M, int N, int K, bool fused = false, bool norm = false) {
+  for (int i = 0; i < h->plan_count; ++i) {
+    const PlanEntry& e = h->plans[i];
+    if (e.M == M && e.N == N && e.K == K && e.fused == fused && e.norm == norm) return e.plan;
+  }
+  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, h->env, fused, norm);
+  const int slot = h->plan_count < kPlanCache ? h->plan_count++ : h->plan_next;
+  if (h->plan_count == kPlanCache) h->plan_next = (slot + 1) % kPlanCache;
+  h->plans[slot] = PlanEntry{M, N, K, fused, norm, plan};
+  return plan;
+}
 
 // 2-D uint8 tensor map over a row-major [rows, k] matrix, box {128 bytes, box_rows}
 // with the 128-byte swizzle; out-of-range rows of a box read as zero.
@@ -100,7 +130,7 @@ int make_tmap(mx_handle* h, CUtensorMap* tm, const void* ptr, int rows, long k, 
   return MX_OK;
 }
 
-int validate_gemm(const mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
+int validate_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scales,
                   const void* w, const void* w_scales) {
   if (M < 1 || N < 1 || K < 1) return MX_ERR_INVALID_ARG;
   if (a == nullptr || a_scales == nullptr || w == nullptr || w_scales == nullptr)
@@ -109,7 +139,7 @@ int validate_gemm(const mx_handle* h, int M, int N, int K, const void* a, const 
     return MX_ERR_INVALID_ARG;
   if (K % 32 != 0) return MX_ERR_INVALID_ARG;
   if (M > 256 || N % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
-  if (mx::plan_gemm(M, N, K, h->sm_count).smem > mx::kMaxDynamicSmem) return MX_ERR_UNSUPPORTED;
+  if (get_plan(h, M, N, K).smem > mx::kMaxDynamicSmem) return MX_ERR_UNSUPPORTED;
   return MX_OK;
 }
 
@@ -129,7 +159,7 @@ int gemm_prepare(mx_handle* h, GemmLaunch* L, int M, int N, int K, const void* a
                  const void* a_scales, const void* w, const void* w_scales, void* out, uint8_t* q,
                  uint8_t* q_scales, int q_cols, const void* x = nullptr, long ldx = 0,
                  int groups = 1, const mx::GemmNorm* norm = nullptr) {
-  L->plan = mx::plan_gemm(M, N, K, h->sm_count, x != nullptr, norm != nullptr);
+  L->plan = get_plan(h, M, N, K, x != nullptr, norm != nullptr);
   int rc = make_tmap(h, &L->tm_w, w, N, K, 128);
   if (rc != MX_OK) return rc;
   if (x != nullptr) {
@@ -195,8 +225,7 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
 int chain_persistent(mx_handle* h, int M, const void* a1, const void* a1_scales, const mx_weight w[3],
                      int g1_cols, void* a2, void* a2_scales, void* a3, void* a3_scales, void* out,
                      void* out1, void* out2, cudaStream_t stream) {
-  const char* e = getenv("MX_CHAIN_PERSISTENT");
-  if (e == nullptr || atoi(e) != 1) return MX_ERR_UNSUPPORTED;
+  if (!h->chain_persistent) return MX_ERR_UNSUPPORTED;
   if (h->chain_clusters < 1) return MX_ERR_UNSUPPORTED;
   mx::ChainArgs args = {};
   const void* acts[3] = {a1, a2, a3};
@@ -211,7 +240,7 @@ int chain_persistent(mx_handle* h, int M, const void* a1, const void* a1_scales,
     P.a_scales = static_cast<const uint8_t*>(act_scales[p]);
     P.n = w[p].n;
     P.k = w[p].k;
-    P.splits = mx::plan_gemm(M, w[p].n, w[p].k, h->sm_count).splits;
+    P.splits = get_plan(h, M, w[p].n, w[p].k).splits;
     P.out = outs[p];
     P.q = qs[p];
     P.q_scales = qscales[p];
@@ -269,6 +298,9 @@ int mx_create(mx_handle** out, int device) {
   } else {
     h->device = device;
     h->sm_count = sms;
+    h->env = mx::read_plan_env();
+    const char* pe = getenv("MX_CHAIN_PERSISTENT");
+    h->chain_persistent = pe != nullptr && atoi(pe) == 1;
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
@@ -383,9 +415,83 @@ int mx_gemm_bf16(mx_handle* h, int M, int N, int K, const void* x, long ldx, con
   if (out == nullptr || !aligned(out, 16)) return MX_ERR_INVALID_ARG;
   if (flags & ~MX_FLAG_PDL) return MX_ERR_INVALID_ARG;
   if (M > 256 || N % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
-  if (mx::plan_gemm(M, N, K, h->sm_count, true).smem > mx::kMaxDynamicSmem) return MX_ERR_UNSUPPORTED;
+  if (get_plan(h, M, N, K, true).smem > mx::kMaxDynamicSmem) return MX_ERR_UNSUPPORTED;
   return gemm_launch(h, M, N, K, nullptr, nullptr, w, w_scales, out, nullptr, nullptr, 0,
                      (flags & MX_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream), x, ldx);
+}
+
+// ------------------------------------------------------------------ warm-up
+namespace {
+
+// One weight per distinct (n, k), in increasing (n, k) order: indices into w.
+std::vector<int> shape_representatives(const mx_weight* w, int nw) {
+  std::vector<int> reps;
+  for (int i = 0; i < nw; ++i) {
+    bool seen = false;
+    for (int j : reps) seen = seen || (w[j].n == w[i].n && w[j].k == w[i].k);
+    if (!seen) reps.push_back(i);
+  }
+  std::sort(reps.begin(), reps.end(), [&](int a, int b) {
+    return w[a].n != w[b].n ? w[a].n < w[b].n : w[a].k < w[b].k;
+  });
+  return reps;
+}
+
+// The zero activation's codes region, its scales region, and the outputs, in bytes.
+bool warmup_layout(const mx_weight* w, int nw, const int* rows, int nrows, size_t* codes,
+                   size_t* scales, size_t* outs) {
+  if (w == nullptr || rows == nullptr || nw < 1 || nrows < 1) return false;
+  *codes = *scales = *outs = 0;
+  for (int i : shape_representatives(w, nw)) {
+    if (w[i].n < 1 || w[i].k < 32 || w[i].k % 32 != 0) return false;
+    for (int j = 0; j < nrows; ++j) {
+      if (rows[j] < 1) return false;
+      *codes = std::max(*codes, static_cast<size_t>(rows[j]) * w[i].k);
+      *scales = std::max(*scales, mx_scale_bytes(rows[j], w[i].k));
+      *outs += round256(static_cast<size_t>(rows[j]) * w[i].n * 2);
+    }
+  }
+  *codes = round256(*codes);
+  *scales = round256(*scales);
+  return true;
+}
+
+}  // namespace
+
+size_t mx_warmup_bytes(const mx_weight* w, int nw, const int* rows, int nrows) {
+  size_t codes, scales, outs;
+  return warmup_layout(w, nw, rows, nrows, &codes, &scales, &outs) ? codes + scales + outs : 0;
+}
+
+int mx_warmup(mx_handle* h, const mx_weight* w, int nw, const int* rows, int nrows, void* scratch,
+              size_t scratch_bytes, void* stream) {
+  int rc = check_device(h);
+  if (rc != MX_OK) return rc;
+  size_t codes, scales, outs;
+  if (!warmup_layout(w, nw, rows, nrows, &codes, &scales, &outs)) return MX_ERR_INVALID_ARG;
+  if (scratch == nullptr || !aligned(scratch, 256) || scratch_bytes < codes + scales + outs)
+    return MX_ERR_INVALID_ARG;
+  uint8_t* const base = static_cast<uint8_t*>(scratch);
+  const std::vector<int> reps = shape_representatives(w, nw);
+  // every launch is validated and prepared (plan, tensor maps) before the first
+  std::vector<GemmLaunch> launches(reps.size() * static_cast<size_t>(nrows));
+  size_t off = codes + scales;
+  for (size_t r = 0; r < reps.size(); ++r) {
+    const mx_weight& wr = w[reps[r]];
+    for (int j = 0; j < nrows; ++j) {
+      rc = validate_gemm(h, rows[j], wr.n, wr.k, base, base + codes, wr.w, wr.w_scales);
+      if (rc == MX_OK)
+        rc = gemm_prepare(h, &launches[r * nrows + j], rows[j], wr.n, wr.k, base, base + codes, wr.w,
+                          wr.w_scales, base + off, nullptr, nullptr, 0);
+      if (rc != MX_OK) return rc;
+      off += round256(static_cast<size_t>(rows[j]) * wr.n * 2);
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the zero MXFP8 activation: zero codes, zero scale bytes (as the mxfp8 page's `_zeros`)
+  rc = cuda_status(cudaMemsetAsync(base, 0, codes + scales, s));
+  for (size_t i = 0; i < launches.size() && rc == MX_OK; ++i) rc = gemm_run(h, &launches[i], true, s);
+  return rc;
 }
 
 int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, const mx_weight w[3],
@@ -449,7 +555,7 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
   // rows, and the stand-alone norm kernel between G1 and G2 is faster.
   const bool fused = M <= kNormFusedMaxRows &&
                      static_cast<size_t>(M) * (g1_cols / 32) * sizeof(float) <= kSsqBytes &&
-                     mx::plan_gemm(M, w[1].n, w[1].k, h->sm_count, true, true).smem <= mx::kMaxDynamicSmem;
+                     get_plan(h, M, w[1].n, w[1].k, true, true).smem <= mx::kMaxDynamicSmem;
   const mx::GemmNorm norm{static_cast<const uint16_t*>(norm_weight), eps, h->d_ssq,
                           static_cast<uint16_t*>(debug_y), static_cast<uint8_t*>(a2),
                           static_cast<uint8_t*>(a2_scales)};
@@ -500,7 +606,7 @@ int woa_two_launch(mx_handle* h, int T, const void* x, long ldx, const int64_t* 
                    void* q, void* q_scales, cudaStream_t s) {
   const int D = d_nope + d_rope;
   const long kx = static_cast<long>(G) * H * D;  // the activation's K (all groups)
-  if (kx > (1L << 30) || mx::plan_gemm(T, G * R, H * D, h->sm_count).smem > mx::kMaxDynamicSmem)
+  if (kx > (1L << 30) || get_plan(h, T, G * R, H * D).smem > mx::kMaxDynamicSmem)
     return MX_ERR_UNSUPPORTED;
   // 1. inverse RoPE + MX quantize of all heads -> xq (swizzled scales over G*H*D)
   const mx::RopeArgs rope{positions, cos_sin, max_pos, D, d_nope, h->d_status};
@@ -545,7 +651,7 @@ int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* po
                         static_cast<cudaStream_t>(stream));
     if (rc != MX_ERR_UNSUPPORTED) return rc;
   }
-  const mx::WoaPlan plan = mx::plan_wo_a(T, G, H, R, h->sm_count);
+  const mx::WoaPlan plan = mx::plan_wo_a(T, G, H, R, h->sm_count, h->env);
   CUtensorMap tm_w;
   rc = make_tmap(h, &tm_w, w, G * R, H * D, 128);
   if (rc != MX_OK) return rc;
@@ -626,8 +732,6 @@ int chain_scratch(int device, uint8_t** out) {
   *out = static_cast<uint8_t*>(g_scratch_address[device]);
   return MX_OK;
 }
-
-size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
 

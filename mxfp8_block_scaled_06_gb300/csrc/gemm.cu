@@ -39,6 +39,8 @@
 
 #include <algorithm>
 
+#include <cstdio>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -115,6 +117,39 @@ struct Layout {
 };
 
 __host__ __device__ inline int tmem_sfa_col(int mtile) { return (mtile + 15) & ~15; }
+
+// The 64 bytes at src (shared memory) into w[0..15] in order, read as four
+// 16-byte loads that start at granule rot (0..3): threads that differ in rot
+// hit different banks. The rotation is undone with selects, so every register
+// index is a compile-time constant.
+__device__ __forceinline__ void load_block64(const uint8_t* src, int rot, uint32_t (&w)[16]) {
+  uint4 r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r[j] = *reinterpret_cast<const uint4*>(src + ((j + rot) & 3) * 16);
+  // r[j] holds granule (j + rot) & 3: granule q is r[(q - rot) & 3]
+  if (rot & 1) {
+    const uint4 t = r[3];
+    r[3] = r[2];
+    r[2] = r[1];
+    r[1] = r[0];
+    r[0] = t;
+  }
+  if (rot & 2) {
+    uint4 t = r[0];
+    r[0] = r[2];
+    r[2] = t;
+    t = r[1];
+    r[1] = r[3];
+    r[3] = t;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    w[4 * q] = r[q].x;
+    w[4 * q + 1] = r[q].y;
+    w[4 * q + 2] = r[q].z;
+    w[4 * q + 3] = r[q].w;
+  }
+}
 
 template <bool kRequant, bool kFusedA>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -258,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* const row_inv = reinterpret_cast<float*>(base_ptr + L.inv);
     const bool norm_out = norm && tile == 0;  // tile 0 writes y and the activation
     const int nblk = p.K >> 5;                // 32-blocks of a whole row (the norm's sum)
-    const int units_per_row = n * 16;         // 8-element units in the K-range
+    const int blocks_per_row = n * 4;         // 32-blocks in the K-range
     for (int r0 = 0, batch = 0; r0 < p.M; r0 += kRowBatch, ++batch) {
       // every thread reads the flag after the previous batch's barrier: once a
       // wait has expired no further row batch is requested
@@ -307,81 +342,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (batch == 0 && threadIdx.x == 0) MX_TL(13, globaltimer());
       }
-      const int total = rb * units_per_row;
+      // one 32-block per thread: its 32 values, amax and codes without shuffles
+      const int total = rb * blocks_per_row;
       const bool go = *abort_flag == 0;
-      // unit u = b0 + threadIdx.x is (row, ul), advanced by kThreads units a pass
-      int row = threadIdx.x / units_per_row, ul = threadIdx.x % units_per_row;
-      const int drow = kThreads / units_per_row, dul = kThreads % units_per_row;
-      for (int b0 = 0; b0 < total; b0 += kThreads) {
-        const bool valid = go && b0 + static_cast<int>(threadIdx.x) < total;
-        const int blk = ul >> 2;  // 32-block within the K-range
-        float v[8];
-        uint32_t amax_bits = 0;  // max |v| as bits: at or above Inf's bits when any is Inf or NaN
-        if (valid) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(base_ptr + L.xraw + row * L.nmax * 256 + ul * 16);
-          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+      int row = threadIdx.x / blocks_per_row, blk = threadIdx.x % blocks_per_row;
+      const int drow = kThreads / blocks_per_row, dblk = kThreads % blocks_per_row;
+      // the four 16-byte loads of a block start at a rotated one (pairs of
+      // threads), so a warp's loads spread over all banks
+      const int rot = (threadIdx.x >> 1) & 3;
+      for (int b0 = 0; go && b0 < total; b0 += kThreads) {
+        if (b0 + static_cast<int>(threadIdx.x) < total) {
+          uint32_t xw[16];
+          load_block64(base_ptr + L.xraw + row * L.nmax * 256 + blk * 64, rot, xw);
+          float v[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[2 * e] = __uint_as_float(w4[e] << 16);
-            v[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+          for (int e = 0; e < 16; ++e) {
+            v[2 * e] = __uint_as_float(xw[e] << 16);
+            v[2 * e + 1] = __uint_as_float(xw[e] & 0xFFFF0000u);
           }
+          const int m = r0 + row;
+          const int kg = c_begin * 128 + blk * 32;  // the block's first column of K
           if (norm) {
             // y = bf16((x * inv_rms) * gamma), as the stand-alone norm kernel
-            const float inv = row_inv[r0 + row];
-            const int kg = c_begin * 128 + ul * 8;
-            const uint4 graw = *reinterpret_cast<const uint4*>(base_ptr + L.gam + ul * 16);
-            const uint32_t g4[4] = {graw.x, graw.y, graw.z, graw.w};
-            uint32_t packed[4];
+            const float inv = row_inv[m];
+            uint32_t gw[16];
+            load_block64(base_ptr + L.gam + blk * 64, rot, gw);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a = __fmul_rn(__fmul_rn(v[2 * e], inv), __uint_as_float(g4[e] << 16));
-              const float b = __fmul_rn(__fmul_rn(v[2 * e + 1], inv), __uint_as_float(g4[e] & 0xFFFF0000u));
+            for (int e = 0; e < 16; ++e) {
+              const float a = __fmul_rn(__fmul_rn(v[2 * e], inv), __uint_as_float(gw[e] << 16));
+              const float b = __fmul_rn(__fmul_rn(v[2 * e + 1], inv), __uint_as_float(gw[e] & 0xFFFF0000u));
               const uint32_t ha = __bfloat16_as_ushort(__float2bfloat16_rn(a));
               const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-              packed[e] = ha | (hb << 16);
+              xw[e] = ha | (hb << 16);
               v[2 * e] = __uint_as_float(ha << 16);
               v[2 * e + 1] = __uint_as_float(hb << 16);
             }
-            if (norm_out && p.norm.y != nullptr)
-              *reinterpret_cast<uint4*>(p.norm.y + static_cast<size_t>(r0 + row) * p.K + kg) =
-                  make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          }
+            if (norm_out && p.norm.y != nullptr) {
+              uint4* const dst = reinterpret_cast<uint4*>(p.norm.y + static_cast<size_t>(m) * p.K + kg);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7FFFFFFFu);
-        }
-        // the four units of a 32-block sit in four consecutive lanes
-        amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, 1));
-        amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, 2));
-        if (valid) {
-          uint32_t sbyte, lo, hi;
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(xw[4 * q], xw[4 * q + 1], xw[4 * q + 2], xw[4 * q + 3]);
+            }
+          }
+          // max |v| as bits: at or above Inf's bits when any value is Inf or NaN
+          uint32_t amax_bits = 0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7FFFFFFFu);
+          uint32_t sbyte;
+          uint32_t cw[8];
           if (amax_bits >= 0x7F800000u) {
             sbyte = 0xFFu;
-            lo = hi = 0x7F7F7F7Fu;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) cw[c] = 0x7F7F7F7Fu;
           } else {
             sbyte = mx_scale_byte(__uint_as_float(amax_bits));
             const float f = mx_inv_scale(sbyte);
-            lo = cvt_e4m3x2(v[0] * f, v[1] * f) | (cvt_e4m3x2(v[2] * f, v[3] * f) << 16);
-            hi = cvt_e4m3x2(v[4] * f, v[5] * f) | (cvt_e4m3x2(v[6] * f, v[7] * f) << 16);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              cw[c] = cvt_e4m3x2(v[4 * c] * f, v[4 * c + 1] * f) | (cvt_e4m3x2(v[4 * c + 2] * f, v[4 * c + 3] * f) << 16);
           }
-          const int m = r0 + row;
-          const int ci = blk >> 2;                       // chunk within the K-range
-          const int kb = (blk & 3) * 32 + (ul & 3) * 8;  // byte within the 128-byte row
-          const uint32_t off = ci * at + (m >> 3) * 1024 + (m & 7) * 128 +
-                               (((kb >> 4) ^ (m & 7)) << 4) + (kb & 15);
-          *reinterpret_cast<uint2*>(base_ptr + L.act + off) = make_uint2(lo, hi);
-          if ((ul & 3) == 0)
-            base_ptr[L.sfb_off(m >> 7, ci) + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (blk & 3)] =
-                static_cast<uint8_t>(sbyte);
+          // the block's 32 codes: two 16-byte granules of the chunk tile's
+          // 128-byte row m, swizzled by m % 8
+          const int ci = blk >> 2;
+          const int g0 = (blk & 3) * 2;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t off = ci * at + (m >> 3) * 1024 + (m & 7) * 128 + (((g0 + hh) ^ (m & 7)) << 4);
+            *reinterpret_cast<uint4*>(base_ptr + L.act + off) =
+                make_uint4(cw[4 * hh], cw[4 * hh + 1], cw[4 * hh + 2], cw[4 * hh + 3]);
+          }
+          base_ptr[L.sfb_off(m >> 7, ci) + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (blk & 3)] =
+              static_cast<uint8_t>(sbyte);
           if (norm_out && p.norm.a_q != nullptr) {
-            const int kg = c_begin * 128 + ul * 8;
-            *reinterpret_cast<uint2*>(p.norm.a_q + static_cast<size_t>(m) * p.K + kg) = make_uint2(lo, hi);
-            if ((ul & 3) == 0) p.norm.a_q_scales[swz_offset(m, kg >> 5, p.K >> 5)] = static_cast<uint8_t>(sbyte);
+            uint4* const dst = reinterpret_cast<uint4*>(p.norm.a_q + static_cast<size_t>(m) * p.K + kg);
+            dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            p.norm.a_q_scales[swz_offset(m, kg >> 5, p.K >> 5)] = static_cast<uint8_t>(sbyte);
           }
         }
         row += drow;
-        ul += dul;
-        if (ul >= units_per_row) {
-          ul -= units_per_row;
+        blk += dblk;
+        if (blk >= blocks_per_row) {
+          blk -= blocks_per_row;
           ++row;
         }
       }
@@ -623,29 +665,72 @@ int pow2_at_least(int v) {
 
 }  // namespace
 
-// K-splits measured on a GB300 (152 SMs) for the projection shapes of the decode
-// step, as back-to-back launches under PDL with weights streamed from HBM: the
-// fastest split count per (N, K) and row range. More CTAs than SMs (two or
-// three co-resident per SM, each with a shallower ring) beat one deep ring per
-// SM as long as the grid fits in one wave. Shapes not listed use the SM-count
-// rule in plan_gemm.
+// K-splits (and, where it helps, the ring depth) of the decode step's projection
+// shapes on a GB300 (152 SMs). G2 and G3 are chosen inside the graph-replayed
+// chain of the three projections (mx_gemm_chain, weights streamed from HBM), as
+// the mxfp8 page picks its fixed tactics per row range in the chain rather than
+// as isolated launches: chain us at M = 4 / 8 / 16 rows went 20.31 -> 19.93,
+// 19.43 -> 19.25 and 20.89 -> 20.58 with these against the previous picks (2, 6
+// and 6 splits for G2, 8 for G3); at one row and from 32 rows on the picks
+// were already the fastest. G1's shape is also the stand-alone GEMM of the
+// benchmark step: in the chain 4 splits with the whole K-range resident save
+// 0.5 us at one to four rows, but cost 0.3 us per stand-alone launch (4.58 ->
+// 4.87 us at M = 1), and one table serves both, so that mx_gemm and the
+// chain's G1 stay the same kernel (the chain equals the composition of its
+// entry points bit for bit); G1 keeps 8 splits. wo_b keeps the counts timed as
+// back-to-back launches. stages = 0: the ring depth plan_gemm derives. Shapes
+// not listed use the SM-count rule in plan_gemm.
 struct SplitEntry {
-  int n, k, max_m, splits;
+  int n, k, max_m, splits, stages;
 };
 constexpr SplitEntry kSplitTable[] = {
-    {2048, 5120, 256, 8},                         // fused_wqa_wkv (G1)
-    {8192, 1536, 4, 2},   {8192, 1536, 256, 6},   // wq_b (G2)
-    {5120, 8192, 32, 8},  {5120, 8192, 256, 6},   // third projection (G3)
-    {5120, 4096, 32, 8},  {5120, 4096, 256, 6},   // wo_b
+    {2048, 5120, 256, 8, 0},                                                     // G1
+    {8192, 1536, 2, 2, 0},    {8192, 1536, 16, 4, 0},   {8192, 1536, 256, 6, 0},  // G2
+    {5120, 8192, 16, 6, 0},   {5120, 8192, 32, 8, 0},   {5120, 8192, 256, 6, 0},  // G3
+    {5120, 4096, 32, 8, 0},   {5120, 4096, 256, 6, 0},                           // wo_b
 };
 
-static int table_splits(int M, int N, int K) {
+static const SplitEntry* table_entry(int M, int N, int K) {
   for (const SplitEntry& e : kSplitTable)
-    if (e.n == N && e.k == K && M <= e.max_m) return e.splits;
-  return 0;
+    if (e.n == N && e.k == K && M <= e.max_m) return &e;
+  return nullptr;
 }
 
-GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a, bool norm) {
+// Tuning override for one weight shape, from MX_PLAN_AT ("NxK:splits[:stages],...",
+// e.g. "8192x1536:4:3"); 0 where the shape is not listed.
+static void plan_override(const char* e, int N, int K, int* splits, int* stages) {
+  *splits = *stages = 0;
+  while (*e != '\0') {
+    int n = 0, k = 0, s = 0, st = 0, used = 0;
+    const int got = sscanf(e, "%dx%d:%d%n:%d%n", &n, &k, &s, &used, &st, &used);
+    if (got < 3) return;
+    if (n == N && k == K) {
+      if (s >= 1 && s <= 16) *splits = s;
+      if (got >= 4 && st >= 1 && st <= 12) *stages = st;
+      return;
+    }
+    e += used;
+    if (*e == ',') ++e;
+  }
+}
+
+PlanEnv read_plan_env() {
+  PlanEnv env{};
+  auto num = [](const char* name, int lo, int hi) {
+    const char* e = getenv(name);
+    const int v = e != nullptr ? atoi(e) : 0;
+    return v >= lo && v <= hi ? v : 0;
+  };
+  env.splits = num("MX_SPLITS", 1, 16);
+  env.stages = num("MX_STAGES", 1, 12);
+  env.woa_splits = num("MX_WOA_SPLITS", 1, 8);
+  if (const char* e = getenv("MX_PLAN_AT")) snprintf(env.plan_at, sizeof(env.plan_at), "%s", e);
+  return env;
+}
+
+GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool fused_a, bool norm) {
+  int force_splits, force_stages;
+  plan_override(env.plan_at, N, K, &force_splits, &force_stages);
   const int mtile = (M + 15) & ~15;
   const int tiles = N / 128;
   const int nchunks = K / 128;
@@ -674,10 +759,8 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a, bool norm) {
     const size_t budget = per_cta <= 8 ? std::min<size_t>(100 * 1024, wave) : wave;
     int stages = budget > scales ? static_cast<int>((budget - scales) / L1.stage_bytes) : 0;
     stages = std::max(2, std::min(stages, 10));
-    if (const char* e = getenv("MX_STAGES")) {
-      const int v = atoi(e);
-      if (v >= 1 && v <= 12) stages = v;
-    }
+    if (env.stages > 0) stages = env.stages;
+    if (force_stages > 0) stages = force_stages;
     stages = std::min(stages, per_cta);
     // the epilogue stages the fp32 partials [mtile][128] over the ring and what follows it
     while (static_cast<size_t>(stages) * L1.stage_bytes + scales < static_cast<size_t>(mtile) * 512)
@@ -694,15 +777,18 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a, bool norm) {
   };
   int splits = std::max(1, sm_count / std::max(tiles, 1));
   // the table was measured with 152 SMs; other parts keep the SM-count rule
-  if (sm_count == 152 && table_splits(M, N, K) > 0) splits = table_splits(M, N, K);
+  const SplitEntry* te = sm_count == 152 ? table_entry(M, N, K) : nullptr;
+  if (te != nullptr) splits = te->splits;
+  if (te != nullptr && force_stages == 0) force_stages = te->stages;
   splits = std::min(splits, std::min(8, nchunks));
   bool forced = false;
-  if (const char* e = getenv("MX_SPLITS")) {
-    const int v = atoi(e);
-    if (v >= 1 && v <= 16) {
-      splits = std::min(v, nchunks);
-      forced = true;
-    }
+  if (env.splits > 0) {
+    splits = std::min(env.splits, nchunks);
+    forced = true;
+  }
+  if (force_splits > 0) {
+    splits = std::min(force_splits, nchunks);
+    forced = true;
   }
   GemmPlan pl = plan_for(splits);
   // An accumulator of more than half the TMEM (mtile above ~230 rows) leaves

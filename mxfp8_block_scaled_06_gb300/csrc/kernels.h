@@ -36,6 +36,18 @@ cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);
 // ------------------------------------------------------------ block-scaled GEMM
 // Plan of one GEMM launch: activation tile (MMA N), K-splits per weight tile
 // (a thread-block cluster along K), pipeline depth, TMEM columns, shared bytes.
+// Plan overrides for tuning, read from the environment once per handle (at
+// mx_create): MX_SPLITS (K-splits of every GEMM), MX_STAGES (ring depth),
+// MX_PLAN_AT ("NxK:splits[:stages],..." for listed weight shapes),
+// MX_WOA_SPLITS (fused WO-A K-splits). Zero / empty = none.
+struct PlanEnv {
+  int splits;
+  int stages;
+  int woa_splits;
+  char plan_at[256];
+};
+PlanEnv read_plan_env();
+
 struct GemmPlan {
   int mtile;
   int splits;
@@ -99,7 +111,8 @@ constexpr int kTimelineCtas = 512;
 #endif
 
 // fused_a: bf16 activations quantized in the kernel; norm: with the RMS norm.
-GemmPlan plan_gemm(int M, int N, int K, int sm_count, bool fused_a = false, bool norm = false);
+GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool fused_a = false,
+                   bool norm = false);
 cudaError_t set_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& args,
                         const GemmPlan& plan, bool pdl, cudaStream_t stream);
@@ -181,7 +194,7 @@ struct WoaArgs {
   int* status;
 };
 
-WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count);
+WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count, const PlanEnv& env);
 cudaError_t set_wo_a_attributes();
 cudaError_t launch_wo_a(const CUtensorMap& tm_w, const WoaArgs& args, const WoaPlan& plan,
                         cudaStream_t stream);

@@ -430,7 +430,7 @@ int pow2_at_least(int v) {
 
 }  // namespace
 
-WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count) {
+WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count, const PlanEnv& env) {
   WoaPlan pl{};
   pl.mtile = (T + 15) & ~15;
   const int tiles = G * (R / 128);
@@ -441,10 +441,7 @@ WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count) {
   const int per_sm = T <= 16 ? 2 : 1;
   int splits = std::max(1, per_sm * sm_count / std::max(tiles, 1));
   splits = std::min(splits, std::min(8, nchunks));
-  if (const char* e = getenv("MX_WOA_SPLITS")) {
-    const int v = atoi(e);
-    if (v >= 1 && v <= 8) splits = std::min(v, nchunks);
-  }
+  if (env.woa_splits > 0) splits = std::min(env.woa_splits, nchunks);
   const int tbmax = std::min(T, kTokenBatch);
   // more K-splits (fewer resident activation chunks) and a shallower weight
   // ring until the CTA fits in shared memory

@@ -68,6 +68,25 @@ def test_scale_bytes_rejects_bad_k(lib):
     assert lib.mx_scale_bytes(-1, 128) == 0
 
 
+def test_warmup_bytes_follows_the_documented_layout(lib):
+    """Host-only: the zero activation (largest rows*k codes, largest scale
+    bytes), then one bf16 output per distinct (n, k) and row count, each
+    rounded to 256 bytes. A repeated shape adds nothing."""
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    shapes = [(2048, 5120), (8192, 1536), (2048, 5120)]
+    ws = (mx.MxWeight * 3)(*[mx.MxWeight(None, None, n, k) for n, k in shapes])
+    rows = (ctypes.c_int * 2)(1, 16)
+    r256 = lambda v: (v + 255) // 256 * 256
+    want = (r256(16 * 5120) + r256(oracle.mx_scale_bytes(16, 5120))
+            + sum(r256(r * n * 2) for n in (2048, 8192) for r in (1, 16)))
+    assert lib.mx_warmup_bytes(ws, 3, rows, 2) == want
+    assert lib.mx_warmup_bytes(ws, 0, rows, 2) == 0
+    assert lib.mx_warmup_bytes(ws, 3, rows, 0) == 0
+    bad = (ctypes.c_int * 1)(0)
+    assert lib.mx_warmup_bytes(ws, 3, bad, 1) == 0
+
+
 def test_status_strings(lib):
     import mxfp8_block_scaled_06_gb300 as mx
 

@@ -148,3 +148,40 @@ def test_empty_inputs_are_rejected_and_launch_nothing():
     for buf, nbytes in g.bufs:  # the outputs themselves are untouched too
         assert (buf[PAD:PAD + nbytes].cpu().numpy() == PATTERN).all()
     assert mx.mx_device_status(handle()) == mx.MX_OK
+
+
+@pytest.mark.parametrize("fault", ["n_not_tiled", "k_mismatch", "scales_misaligned"])
+def test_chain_rejecting_its_third_projection_writes_nothing(fault):
+    """A chain whose third projection is rejected fails before its first launch:
+    out1 / out2, a2, a3 and out keep every byte (the cute_dsl page's `_consumer`
+    validates before any launch). Called through the C ABI, so the binding's own
+    checks do not stand in front of the library's."""
+    import mxfp8_block_scaled_06_gb300 as mx
+
+    lib, h = mx.load_library(), handle().ptr
+    m, (n1, k1), (n2, k2), (n3, k3) = 4, (384, 640), (256, 256), (512, 256)
+    w = [quantize_on_gpu(synth.block_scaled_bf16(7 + i, synth.TAG_W, n, k, -6, 6))
+         for i, (n, k) in enumerate([(n1, k1), (n2, k2), (n3, k3)])]
+    aq, asc = quantize_on_gpu(synth.block_scaled_bf16(7, synth.TAG_A, m, k1, -4, 4))
+    nw = torch.ones(k2, dtype=torch.bfloat16, device="cuda")
+    p = lambda t: t.data_ptr()
+    third = {"n_not_tiled": (p(w[2][0]), p(w[2][1]), n3 + 64, k3, mx.MX_ERR_UNSUPPORTED),
+             "k_mismatch": (p(w[2][0]), p(w[2][1]), n3, k3 + 128, mx.MX_ERR_INVALID_ARG),
+             "scales_misaligned": (p(w[2][0]), p(w[2][1]) + 16, n3, k3, mx.MX_ERR_INVALID_ARG)}[fault]
+    ws = (mx.MxWeight * 3)(mx.MxWeight(p(w[0][0]), p(w[0][1]), n1, k1),
+                           mx.MxWeight(p(w[1][0]), p(w[1][1]), n2, k2),
+                           mx.MxWeight(*third[:4]))
+    g = Guarded()
+    out1, out2, out = g.u8(m * n1 * 2), g.u8(m * n2 * 2), g.u8(m * (n3 + 64) * 2)
+    a2, a2s = g.u8(m * k2), g.u8(mx.mx_scale_bytes(m, k2))
+    a3, a3s = g.u8(m * n2), g.u8(mx.mx_scale_bytes(m, n2))
+    y = g.u8(m * k2 * 2)
+    torch.cuda.synchronize()
+    assert lib.mx_gemm_chain(h, m, p(aq), p(asc), ws, k2, p(a2), p(a2s), p(a3), p(a3s), p(out),
+                             p(out1), p(out2), None) == third[4]
+    assert lib.mx_gemm_chain_norm(h, m, p(aq), p(asc), ws, k2, p(nw), 1e-6, p(out1), p(a2), p(a2s),
+                                  p(a3), p(a3s), p(out), p(y), p(out2), None) == third[4]
+    g.check()
+    for buf, nbytes in g.bufs:
+        assert (buf[PAD:PAD + nbytes].cpu().numpy() == PATTERN).all(), "a rejected chain wrote an output"
+    assert mx.mx_device_status(handle()) == mx.MX_OK

@@ -52,15 +52,16 @@ def _dequant_torch(codes: np.ndarray, plain_scales: np.ndarray) -> np.ndarray:
     return (v.reshape(m, k // 32, 32) * s[..., None]).reshape(m, k).numpy()
 
 
-def _run_chain(m, shapes, g1_cols, seed):
+def _run_chain(m, shapes, g1_cols, seed, h=None):
     import mxfp8_block_scaled_06_gb300 as mx
 
+    h = h or handle()
     ws = _weights(shapes, seed)
     a_bits, _, (ra, rsa) = operands(seed, synth.TAG_A, m, shapes[0][1], -4, 4)
     aq, asc = quantize_on_gpu(a_bits)
-    res = mx.mx_gemm_chain(handle(), aq, asc, [w[0] for w in ws], g1_cols=g1_cols, debug=True)
+    res = mx.mx_gemm_chain(h, aq, asc, [w[0] for w in ws], g1_cols=g1_cols, debug=True)
     torch.cuda.synchronize()
-    assert mx.mx_device_status(handle()) == mx.MX_OK
+    assert mx.mx_device_status(h) == mx.MX_OK
     return ws, (aq, asc), (ra, rsa), res
 
 
@@ -74,10 +75,10 @@ def test_chain_equals_composition_decode_shapes(m):
     _composition(m, [(2048, 5120), (8192, 1536), (5120, 8192)], 1536, seed=2)
 
 
-def _composition(m, shapes, g1_cols, seed):
+def _composition(m, shapes, g1_cols, seed, chain_handle=None):
     import mxfp8_block_scaled_06_gb300 as mx
 
-    ws, (aq, asc), _, res = _run_chain(m, shapes, g1_cols, seed)
+    ws, (aq, asc), _, res = _run_chain(m, shapes, g1_cols, seed, chain_handle)
     h = handle()
     o1 = mx.mx_gemm(h, aq, asc, *ws[0][0])
     a2, a2s = mx.mx_quantize_rows(h, o1[:, :g1_cols])
@@ -102,8 +103,8 @@ def test_chain_vs_oracle_small(m):
     _vs_oracle(m, [(384, 640), (256, 256), (512, 256)], 256, seed=9)
 
 
-def _vs_oracle(m, shapes, g1_cols, seed):
-    ws, _, (ra, rsa), res = _run_chain(m, shapes, g1_cols, seed)
+def _vs_oracle(m, shapes, g1_cols, seed, chain_handle=None):
+    ws, _, (ra, rsa), res = _run_chain(m, shapes, g1_cols, seed, chain_handle)
     ora = oracle.chain(ra, rsa, [w[1] for w in ws], g1_cols=g1_cols)
     assert_gemm_close(res["out1"], ora["out1"], "chain G1")
     prev_codes, prev_scales = None, None

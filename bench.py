@@ -755,12 +755,20 @@ def run_timeline(args):
             h, q1[0], q1[1], cw[i % cset], nw, 1e-6, g1_cols=CHAIN_G1_COLS, out1=out1, stream=stream,
             **bufs), 4, period=3,
             names=("G1", "G2+norm", "G3") if m <= 16 else ("G1", "G2 (after the norm kernel)", "G3"))
+    for n, k in SWEEP_SHAPES:
+        ws = rig.weight_set([(n, k)], seed=4, ncopies=rig.copies(w_bytes(n, k)))
+        for m in (32, 64, 128, 192, 256):
+            q = mx.mx_quantize_rows(h, rig.activation(m, k, seed=4))
+            o = torch.empty((m, n), dtype=torch.bfloat16, device=rig.dev)
+            out[f"gemm_M{m}_N{n}_K{k}"] = record(
+                lambda i, q=q, o=o, ws=ws: mx.mx_gemm(h, q[0], q[1], *ws[i % len(ws)][0], out=o, pdl=True,
+                                                      stream=stream), 6)
     torch.cuda.synchronize()
     assert mx.mx_device_status(h) == mx.MX_OK
     print(json.dumps({"timeline": out}))
 
 
-TUNE_M = (1, 2, 4, 8, 16, 32, 48, 64)
+TUNE_M = (1, 2, 4, 8, 16, 32, 48, 64, 96, 128, 192, 256)
 
 
 def run_tune_chain(args):
@@ -788,7 +796,7 @@ def run_tune_chain(args):
     spec = lambda picks: ",".join(f"{n}x{k}:{s}" + (f":{st}" if st else "")
                                   for (n, k), (s, st) in picks.items())
     out = {}
-    for m in TUNE_M:
+    for m in (TUNE_M if not args.tune_rows else [int(v) for v in args.tune_rows.split(",")]):
         q1 = mx.mx_quantize_rows(h, rig.activation(m, CHAIN_SHAPES[0][1], seed=2, umin=-4, umax=4))
         bufs = dict(out=torch.empty((m, CHAIN_SHAPES[2][0]), dtype=torch.bfloat16, device=rig.dev),
                     a2=torch.empty((m, CHAIN_G1_COLS), dtype=torch.uint8, device=rig.dev),
@@ -877,6 +885,7 @@ def main():
                     help="per-CTA phase timeline of GEMM launches (builds the -DMX_TIMELINE library)")
     ap.add_argument("--tune-chain", action="store_true",
                     help="time each chain projection's K-split / ring-depth candidates inside the chain")
+    ap.add_argument("--tune-rows", default="", help="row counts for --tune-chain, e.g. 64,128")
     ap.add_argument("--replica-selftest", action="store_true",
                     help="the replicas' host-side coordination only (no GPU), e.g. with --gpus 2")
     args = ap.parse_args()

@@ -37,7 +37,7 @@ cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);
 // Plan of one GEMM launch: activation tile (MMA N), K-splits per weight tile
 // (a thread-block cluster along K), pipeline depth, TMEM columns, shared bytes.
 // Plan overrides for tuning, read from the environment once per handle (at
-// mx_create): MX_SPLITS (K-splits of every GEMM), MX_STAGES (ring depth),
+// mx_create): MX_SPLITS (K-splits of every GEMM, 1..8), MX_STAGES (ring depth),
 // MX_PLAN_AT ("NxK:splits[:stages],..." for listed weight shapes),
 // MX_WOA_SPLITS (fused WO-A K-splits). Zero / empty = none.
 struct PlanEnv {

@@ -168,6 +168,14 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
+// 16 bytes from a peer CTA's shared memory (16-byte aligned), as above.
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
 // Sum of the float at shared offset `addr` over cluster ranks 0..S-1 (S <= 16),
 // in rank order; the loads of each group of 8 ranks are issued before their adds.
 __device__ __forceinline__ float cluster_sum(uint32_t addr, int S) {

@@ -122,8 +122,9 @@ __host__ __device__ inline int tmem_sfa_col(int mtile) { return (mtile + 15) & ~
 // Whether the epilogue reduces whole rows per warp (16-byte peer loads) rather
 // than 32-column items: measured on GB300, 3-4x faster with two or three K-splits
 // once a warp has two or more rows (N = 8192, K = 5120, M = 128: 9.5 -> 3.0 us),
-// no faster with six (N = 5120, K = 8192, M = 192: 6.5 -> 6.4 us).
-inline bool row_reduction(int M, int splits) { return splits <= 3 && M >= 8 * splits; }
+// no faster with six (N = 5120, K = 8192, M = 192: 6.5 -> 6.4 us); the peer loads
+// of up to four ranks are issued together.
+inline bool row_reduction(int M, int splits) { return splits <= 4 && M >= 8 * splits; }
 
 // The 64 bytes at src (shared memory) into w[0..15] in order, read as four
 // 16-byte loads that start at granule rot (0..3): threads that differ in rot
@@ -633,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (use[b]) emit(i0 + b * 4 * S, sums[b]);  // use[] is warp-uniform
       }
     } else {
-      // Several rows per warp and at most three K-splits (row_reduction): a
+      // Several rows per warp and at most four K-splits (row_reduction): a
       // warp reduces whole rows of the tile, lane l owning columns 4l .. 4l + 3,
       // with 16-byte peer loads; the loads of kRedRows rows x 4 ranks are in
       // flight at once, each column still summed in rank order. Row m goes to
@@ -766,28 +767,29 @@ int pow2_at_least(int v) {
 }  // namespace
 
 // K-splits (and, where it helps, the ring depth) of the decode step's projection
-// shapes on a GB300 (152 SMs). G2 and G3 are chosen inside the graph-replayed
-// chain of the three projections (mx_gemm_chain, weights streamed from HBM), as
-// the mxfp8 page picks its fixed tactics per row range in the chain rather than
-// as isolated launches: chain us at M = 4 / 8 / 16 rows went 20.31 -> 19.93,
-// 19.43 -> 19.25 and 20.89 -> 20.58 with these against the previous picks (2, 6
-// and 6 splits for G2, 8 for G3); at one row and from 32 rows on the picks
-// were already the fastest. G1's shape is also the stand-alone GEMM of the
-// benchmark step: in the chain 4 splits with the whole K-range resident save
-// 0.5 us at one to four rows, but cost 0.3 us per stand-alone launch (4.58 ->
-// 4.87 us at M = 1), and one table serves both, so that mx_gemm and the
-// chain's G1 stay the same kernel (the chain equals the composition of its
-// entry points bit for bit); G1 keeps 8 splits. wo_b keeps the counts timed as
-// back-to-back launches. stages = 0: the ring depth plan_gemm derives. Shapes
-// not listed use the SM-count rule in plan_gemm.
+// shapes on a GB300 (152 SMs), chosen inside the graph-replayed chain of the
+// three projections (bench.py --tune-chain: mx_gemm_chain, weights streamed from
+// HBM), as the mxfp8 page picks its fixed tactics per row range in the chain
+// rather than as isolated launches. Chain us, the table timed as back-to-back
+// launches -> this one: 1 row 19.5 -> 18.5, 4 rows 20.3 -> 18.5, 16 rows
+// 20.9 -> 20.6, 32 rows 23.9 -> 22.7, 64 rows 29.6 -> 26.8, 128 rows 50.8 ->
+// 34.0, 192 rows 77.4 -> 42.6, 256 rows 55.5 -> 49.3 (from 32 rows four or
+// fewer splits win once their partials are reduced as whole rows). G1's shape
+// is also the stand-alone GEMM of the benchmark step: in the chain 4 splits with
+// the whole K-range resident save 0.5 us at one to four rows but cost 0.3 us per
+// stand-alone launch (4.58 -> 4.87 us at M = 1), and one table serves both, so
+// that mx_gemm and the chain's G1 stay the same kernel (the chain equals the
+// composition of its entry points bit for bit); G1 keeps 8 splits up to 16
+// rows. wo_b keeps the counts timed as back-to-back launches. stages = 0: the
+// ring depth plan_gemm derives. Shapes not listed use the SM-count rule.
 struct SplitEntry {
   int n, k, max_m, splits, stages;
 };
 constexpr SplitEntry kSplitTable[] = {
-    {2048, 5120, 256, 8, 0},                                                     // G1
-    {8192, 1536, 2, 2, 0},    {8192, 1536, 16, 4, 0},   {8192, 1536, 256, 6, 0},  // G2
-    {5120, 8192, 16, 6, 0},   {5120, 8192, 32, 8, 0},   {5120, 8192, 256, 6, 0},  // G3
-    {5120, 4096, 32, 8, 0},   {5120, 4096, 256, 6, 0},                           // wo_b
+    {2048, 5120, 16, 8, 0},   {2048, 5120, 256, 4, 0},                            // G1
+    {8192, 1536, 2, 2, 0},    {8192, 1536, 128, 4, 0},  {8192, 1536, 256, 2, 0},  // G2
+    {5120, 8192, 64, 6, 0},   {5120, 8192, 256, 3, 0},                            // G3
+    {5120, 4096, 32, 8, 0},   {5120, 4096, 256, 6, 0},                            // wo_b
 };
 
 static const SplitEntry* table_entry(int M, int N, int K) {

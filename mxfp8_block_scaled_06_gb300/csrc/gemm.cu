@@ -277,6 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = threadIdx.x; idx < n * nsfb * 32; idx += kThreads)
       *reinterpret_cast<uint4*>(base_ptr + L.sfb_off(idx / (n * 32), 0) + (idx % (n * 32)) * 16) =
           make_uint4(0, 0, 0, 0);
+    // every zero is stored before any thread writes the quantized activation
+    // (after the wait) over the same bytes
+    __syncthreads();
   }
   pdl_wait();
   if (threadIdx.x == 0) MX_TL(4, globaltimer());

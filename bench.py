@@ -625,7 +625,8 @@ def run_profile(args):
 
 
 TIMELINE_SLOTS = {"entry": 0, "setup": 1, "w_issued": 2, "wsf_landed": 3, "wait_ret": 4,
-                  "rms_done": 13, "x_landed": 14, "act_quantized": 12, "first_full": 5, "accum": 6, "red_pass": 7, "red_done": 8,
+                  "rms_done": 13, "x_landed": 14, "act_quantized": 12, "first_full": 5, "last_full": 15,
+                  "second_full": 18, "mma_issued": 16, "accum": 6, "red_pass": 7, "red_done": 8,
                   "exit": 9}
 TIMELINE_EXIT = TIMELINE_SLOTS["exit"]
 
@@ -647,7 +648,7 @@ def run_timeline(args):
     lib.mx_timeline_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                      ctypes.POINTER(ctypes.c_int)]
     lib.mx_timeline_reset.argtypes = [ctypes.c_void_p]
-    ctas, slots, launches = 512, 16, 256
+    ctas, slots, launches = 512, 20, 256
     torch.cuda.set_device(0)
     h = mx.mx_create(0)
     props = torch.cuda.get_device_properties(0)
@@ -701,7 +702,10 @@ def run_timeline(args):
                     if len(v):
                         phases[k].append(float(np.median(v)))
                         spread[k].append(float(v.max() - v.min()))
+            landed = [float(np.median(tl[i][tl[i][:, e] > 0][:, 17])) for i in range(max(1, pos), len(tl), period)
+                      if (tl[i][:, e] > 0).any()]
             res[names[pos] if names else pos] = {
+                "stages_landed_at_wait_median": float(np.median(landed)) if landed else None,
                 "launch_us_median": round(float(np.median(dur)), 3) if dur else None,
                 "ctas_started_before_previous_end": round(float(np.median(early)), 3) if early else None,
                 "weight_scales_landed_before_previous_end": round(float(np.median(landed_early)), 3)

@@ -55,7 +55,9 @@ constexpr int kThreads = 128;
 // returned, 5 first chunk landed, 6 accumulator complete, 7 reduction barrier
 // passed, 8 reduction done, 9 exit, 10 SM id, 11 chunks in the K-range,
 // 12 bf16 activations quantized, 13 RMS of the rows done, 14 first row batch
-// landed (12-14: in-kernel quantization only).
+// landed (12-14: in-kernel quantization only), 15 last chunk landed, 16 every
+// MMA issued, 17 ring stages already landed when the wait returned (a count),
+// 18 second chunk landed.
 #ifdef MX_TIMELINE
 #define MX_TL(slot, v)                                                             \
   do {                                                                             \
@@ -283,6 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   pdl_wait();
   if (threadIdx.x == 0) MX_TL(4, globaltimer());
+#ifdef MX_TIMELINE
+  // ring stages whose copies had all landed when the wait returned
+  if (warp == 1 && lane == 0) {
+    unsigned long long landed = 0;
+    for (int s = 0; s < min(n, stages); ++s) landed += mbar_test_wait(full(s), 0) ? 1 : 0;
+    MX_TL(17, landed);
+  }
+#endif
 
   // ---------------- activations (written by the previous kernel on the stream)
   int x_batches = 0;  // bf16 row batches requested (fused), warp 3
@@ -510,6 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (i == 0 && lane == 0) MX_TL(5, globaltimer());
+        if (i == 1 && lane == 0) MX_TL(18, globaltimer());
+        if (i == n - 1 && lane == 0) MX_TL(15, globaltimer());
         tc_fence_after();
         if (elect_one()) {
           tmem_cp_32x128b_x4_lh(ta, f_lo, sf_hi);
@@ -546,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (elect_one()) tc_commit(accum_bar);
     __syncwarp();
+    if (lane == 0) MX_TL(16, globaltimer());
   }
   __syncwarp();
 

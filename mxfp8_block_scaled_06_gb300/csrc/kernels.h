@@ -106,7 +106,7 @@ struct GemmArgs {
 
 #ifdef MX_TIMELINE
 // Timeline build only: stamps per CTA of one GEMM launch (see gemm.cu).
-constexpr int kTimelineSlots = 16;
+constexpr int kTimelineSlots = 20;
 constexpr int kTimelineCtas = 512;
 #endif
 

@@ -826,17 +826,22 @@ def run_tune_chain(args):
 
         current = timed("")
         picks, cands = {}, {}
-        for n, k in CHAIN_SHAPES:
-            times = {}
-            for s in range(1, min(8, k // 128) + 1):
-                for st in (0, 12):  # 0: ring depth as planned; 12: the whole K-range resident
-                    try:
-                        times[(s, st)] = timed(spec({**picks, (n, k): (s, st)}))
-                    except mx.MxError:  # no plan fits shared memory: the library rejects it
-                        pass
-            best = min(times, key=times.get)
-            picks[(n, k)] = best
-            cands[f"{n}x{k}"] = {f"s{s}" + ("_deep" if st else ""): round(t, 3) for (s, st), t in times.items()}
+        # ring depth candidates: 0 = as planned, 3 = shallow (room for the next
+        # kernel's CTAs beside this one's), 12 = the whole K-range resident
+        depths = (0, 3, 12) if args.tune_rounds > 1 else (0, 12)
+        for rnd in range(args.tune_rounds):
+            for n, k in CHAIN_SHAPES:
+                times = {}
+                for s in range(1, min(8, k // 128) + 1):
+                    for st in depths:
+                        try:
+                            times[(s, st)] = timed(spec({**picks, (n, k): (s, st)}))
+                        except mx.MxError:  # no plan fits shared memory: the library rejects it
+                            pass
+                best = min(times, key=times.get)
+                picks[(n, k)] = best
+                cands[f"{n}x{k}" + (f"_round{rnd + 1}" if args.tune_rounds > 1 else "")] = {
+                    f"s{s}" + (f"_st{st}" if st else ""): round(t, 3) for (s, st), t in times.items()}
         tuned = timed(spec(picks))
         out[m] = {"current_us": round(current, 3), "tuned_us": round(tuned, 3), "MX_PLAN_AT": spec(picks),
                   "candidates_us": cands}
@@ -890,6 +895,8 @@ def main():
     ap.add_argument("--tune-chain", action="store_true",
                     help="time each chain projection's K-split / ring-depth candidates inside the chain")
     ap.add_argument("--tune-rows", default="", help="row counts for --tune-chain, e.g. 64,128")
+    ap.add_argument("--tune-rounds", type=int, default=1,
+                    help="greedy rounds of --tune-chain (more than one also tries a 3-stage ring)")
     ap.add_argument("--replica-selftest", action="store_true",
                     help="the replicas' host-side coordination only (no GPU), e.g. with --gpus 2")
     args = ap.parse_args()

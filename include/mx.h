@@ -146,9 +146,11 @@ int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scal
  * Constraints: as mx_gemm; MX_ERR_UNSUPPORTED also when the K-range's
  * quantized rows do not fit in one CTA's shared memory (large M with few
  * K-splits): the caller then uses mx_quantize_rows + mx_gemm.
- * Cost: every CTA quantizes the K-range it contracts, so the N/128 weight
- * tiles repeat that work; it saves a launch and wins at one or two rows, while
- * from about four rows on the two-launch path is faster (measured on GB300). */
+ * Cost: every CTA quantizes the K-range it contracts (one 32-block per
+ * thread), so the N/128 weight tiles repeat that work; it saves a launch, and
+ * on GB300 at N = 2048, K = 5120 it is faster than mx_quantize_rows + mx_gemm
+ * from one to eight rows (5.0 / 5.1 / 5.2 / 5.8 us at 1 / 2 / 4 / 8 rows
+ * against 5.8 / 5.9 / 5.9 / 5.9 us). */
 int mx_gemm_bf16(mx_handle* h, int M, int N, int K, const void* x, long ldx,
                  const void* w, const void* w_scales, void* out, unsigned flags,
                  void* stream);

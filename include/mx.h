@@ -8,8 +8,12 @@
  * `compile_low_latency`: Float8E4M3FN operands, Float8E8M0FNU scales, bf16 out).
  *
  * Conventions shared by every entry point:
- *  - Every data pointer is a DEVICE pointer owned by the caller. No call
- *    allocates or frees memory. mx_create allocates the handle's device memory
+ *  - Every data pointer is a DEVICE pointer owned by the caller, except that the
+ *    bf16 input x of mx_quantize_rows and the bf16 output out of mx_gemm may
+ *    also be host memory the device addresses directly (pinned: cudaHostAlloc,
+ *    cudaHostRegister): those kernels touch them with plain loads and stores,
+ *    so a step can read its activations from and write its results to the host
+ *    without copy-engine transfers. No call allocates or frees memory. mx_create allocates the handle's device memory
  *    once: a status word, the per-tile counters of the persistent chain kernel
  *    (64 KiB), the activation scratch of wo_a_grouped's two-launch form
  *    (8.25 MiB) and the block sums of squares of mx_gemm_chain_norm's

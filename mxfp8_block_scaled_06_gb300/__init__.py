@@ -171,12 +171,18 @@ def _sbytes(rows: int, k: int) -> int:
     return (rows + 127) // 128 * 128 * ((k // 32 + 3) // 4 * 4)
 
 
-def _resident(h: Handle, **tensors) -> None:
+def _resident(h: Handle, host_ok=(), **tensors) -> None:
     """Every given tensor lives on the handle's GPU (checked after all the others,
-    so a host tensor is only ever rejected here)."""
+    so a host tensor is only ever rejected here); those named in host_ok may also
+    be pinned host memory, which the kernels address directly (zero-copy)."""
     for name, t in tensors.items():
-        if t is not None and (t.get_device() != h.device or not t.is_cuda):
-            raise ValueError(f"{name}: on {t.device}, the handle's device is cuda:{h.device}")
+        if t is None:
+            continue
+        if name in host_ok and t.device.type == "cpu" and t.is_pinned():
+            continue
+        if t.get_device() != h.device or not t.is_cuda:
+            raise ValueError(f"{name}: on {t.device}, the handle's device is cuda:{h.device}"
+                             + (" (or pinned host memory)" if name in host_ok else ""))
 
 
 def _flat(name: str, t, dtypes, numel: int):
@@ -221,17 +227,25 @@ def _weight(i, w, s):
 
 
 def mx_quantize_rows(h: Handle, x, q=None, scales=None, swizzled: bool = True, stream=None):
-    """bf16 [M, K] (row stride x.stride(0)) -> (E4M3 codes uint8 [M, K], scale bytes)."""
+    """bf16 [M, K] (row stride x.stride(0)) -> (E4M3 codes uint8 [M, K], scale bytes).
+    x may be on the handle's GPU or in pinned host memory (read directly)."""
     import torch
     if x.dim() != 2:
         raise ValueError("x: a 2-D [M, K] tensor is required")
     m, k = x.shape
     _matrix("x", x, (torch.bfloat16,), m, k, row_stride=True)
     sbytes = _sbytes(m, k) if swizzled else m * (k // 32)
-    q = _empty_u8((m, k), x.device) if q is None else _matrix("q", q, _codes_types(), m, k)
     shape = (sbytes,) if swizzled else (m, k // 32)
-    scales = _empty_u8(shape, x.device) if scales is None else _flat("scales", scales, _scale_types(), sbytes)
-    _resident(h, x=x, q=q, scales=scales)
+    if q is not None:
+        _matrix("q", q, _codes_types(), m, k)
+    if scales is not None:
+        _flat("scales", scales, _scale_types(), sbytes)
+    if q is None or scales is None:  # outputs to allocate: x must be usable first
+        _resident(h, host_ok=("x",), x=x)
+    dev = x.device if x.is_cuda else torch.device("cuda", h.device)  # x may be pinned host memory
+    q = _empty_u8((m, k), dev) if q is None else q
+    scales = _empty_u8(shape, dev) if scales is None else scales
+    _resident(h, host_ok=("x",), x=x, q=q, scales=scales)
     _check(load_library().mx_quantize_rows(h.ptr, m, k, _ptr(x), x.stride(0), _ptr(q),
                                            _ptr(scales), int(swizzled), _stream(stream)),
            "mx_quantize_rows")
@@ -240,7 +254,8 @@ def mx_quantize_rows(h: Handle, x, q=None, scales=None, swizzled: bool = True, s
 
 def mx_gemm(h: Handle, a, a_scales, w, w_scales, out=None, m: int | None = None,
             pdl: bool = False, stream=None):
-    """out[M, N] bf16 = dequant(a[M, K]) x dequant(w[N, K])^T (M = a's rows unless m is given)."""
+    """out[M, N] bf16 = dequant(a[M, K]) x dequant(w[N, K])^T (M = a's rows unless m is given);
+    out may be on the handle's GPU or in pinned host memory (written directly)."""
     import torch
     n, k = _weight(0, w, w_scales)
     m = a.shape[0] if m is None else m
@@ -249,7 +264,7 @@ def mx_gemm(h: Handle, a, a_scales, w, w_scales, out=None, m: int | None = None,
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=w.device)
     _matrix("out", out, (torch.bfloat16,), m, n)
-    _resident(h, a=a, a_scales=a_scales, w=w, w_scales=w_scales, out=out)
+    _resident(h, host_ok=("out",), a=a, a_scales=a_scales, w=w, w_scales=w_scales, out=out)
     _check(load_library().mx_gemm(h.ptr, m, n, k, _ptr(a), _ptr(a_scales), _ptr(w), _ptr(w_scales),
                                   _ptr(out), MX_FLAG_PDL if pdl else 0, _stream(stream)), "mx_gemm")
     return out

@@ -134,3 +134,13 @@ def test_python_scale_size_matches_the_library(mx):
     for rows in (0, 1, 5, 127, 128, 129, 300):
         for k in (0, 16, 32, 96, 128, 160, 5120, 8200):
             assert mx._sbytes(rows, k) == mx.mx_scale_bytes(rows, k), (rows, k)
+
+
+def test_unpinned_host_memory_is_refused_where_pinned_is_accepted(mx, h):
+    # x of mx_quantize_rows and out of mx_gemm may be pinned host memory; a plain
+    # (pageable) host tensor is still refused before any call
+    with pytest.raises(ValueError, match="pinned host memory"):
+        mx.mx_quantize_rows(h, bf16(4, 512))
+    args = gemm_args(mx)
+    with pytest.raises(ValueError, match="cuda:0"):
+        mx.mx_gemm(h, **args)

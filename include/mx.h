@@ -153,8 +153,8 @@ int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scal
  * Cost: every CTA quantizes the K-range it contracts (one 32-block per
  * thread), so the N/128 weight tiles repeat that work; it saves a launch, and
  * on GB300 at N = 2048, K = 5120 it is faster than mx_quantize_rows + mx_gemm
- * from one to eight rows (5.0 / 5.1 / 5.2 / 5.8 us at 1 / 2 / 4 / 8 rows
- * against 5.8 / 5.9 / 5.9 / 5.9 us). */
+ * from one to four rows (4.65 / 4.71 / 4.84 us at 1 / 2 / 4 rows against
+ * 5.12 / 5.18 / 5.28 us), slower at eight (5.57 against 5.34 us). */
 int mx_gemm_bf16(mx_handle* h, int M, int N, int K, const void* x, long ldx,
                  const void* w, const void* w_scales, void* out, unsigned flags,
                  void* stream);

@@ -29,6 +29,7 @@ constexpr int kTmapCache = 32;
 struct PlanEntry {
   int M, N, K;
   bool fused, norm;
+  int push_mode;
   mx::GemmPlan plan;
 };
 constexpr int kPlanCache = 64;
@@ -36,6 +37,8 @@ constexpr int kPlanCache = 64;
 struct mx_handle {
   int device;
   int sm_count;
+  size_t smem_per_sm;    // shared memory of an SM, and the reserve of each resident block
+  size_t smem_reserved;
   mx::PlanEnv env;        // plan overrides, read once at mx_create
   bool chain_persistent;  // MX_CHAIN_PERSISTENT=1 at mx_create
   PlanEntry plans[kPlanCache];
@@ -93,16 +96,61 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 
 // The GEMM plan of a problem, computed once per handle (mx_warmup computes those
 // of the registered shapes ahead of the first call).
-mx::GemmPlan get_plan(mx_handle* h, int M, int N, int K, bool fused = false, bool norm = false) {
+mx::GemmPlan get_plan(mx_handle* h, int M, int N, int K, bool fused = false, bool norm = false,
+                      int push_mode = mx::kPushFull) {
   for (int i = 0; i < h->plan_count; ++i) {
     const PlanEntry& e = h->plans[i];
-    if (e.M == M && e.N == N && e.K == K && e.fused == fused && e.norm == norm) return e.plan;
+    if (e.M == M && e.N == N && e.K == K && e.fused == fused && e.norm == norm && e.push_mode == push_mode)
+      return e.plan;
   }
-  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, h->env, fused, norm);
+  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, h->env, fused, norm, push_mode);
   const int slot = h->plan_count < kPlanCache ? h->plan_count++ : h->plan_next;
   if (h->plan_count == kPlanCache) h->plan_next = (slot + 1) % kPlanCache;
-  h->plans[slot] = PlanEntry{M, N, K, fused, norm, plan};
+  h->plans[slot] = PlanEntry{M, N, K, fused, norm, push_mode, plan};
   return plan;
+}
+
+// A chain projection's plan, for the co-residency check below.
+struct ChainShape {
+  int N, K;
+  bool fused, norm;
+};
+
+// The push reduction of each projection of a three-launch chain (PushMode).
+// Under PDL the next grid's CTAs start while the previous grid's still run, on
+// the same SMs when both fit (shared memory, with the per-block reserve, and
+// TMEM). For every pair of neighbours (G3 of the previous step before G1) that
+// fits without the push reduction's receive areas, the chosen forms must fit
+// too: where they do not, the later projection steps down first (full receive
+// area, then the compact one, then none).
+void chain_push(mx_handle* h, int M, const ChainShape (&c)[3], int (&mode)[3]) {
+  auto plan = [&](int i, int m) { return get_plan(h, M, c[i].N, c[i].K, c[i].fused, c[i].norm, m); };
+  auto fits = [&](int pi, int pm, int i, int im) {
+    const mx::GemmPlan prev = plan(pi, pm), next = plan(i, im);
+    const int grid = c[pi].N / 128 * prev.splits;
+    const size_t k = static_cast<size_t>((grid + h->sm_count - 1) / h->sm_count);
+    return k * (prev.smem + h->smem_reserved) + next.smem + h->smem_reserved <= h->smem_per_sm &&
+           k * prev.tmem_cols + next.tmem_cols <= 512;
+  };
+  auto mode_of = [](const mx::GemmPlan& pl) {
+    return pl.reduction == mx::kReducePush          ? mx::kPushFull
+           : pl.reduction == mx::kReducePushCompact ? mx::kPushCompact
+                                                    : mx::kPushNone;
+  };
+  for (int i = 0; i < 3; ++i) mode[i] = mode_of(plan(i, mx::kPushFull));
+  for (bool changed = true; changed;) {  // each pass steps one down, or ends
+    changed = false;
+    for (int i = 0; i < 3 && !changed; ++i) {
+      const int pi = (i + 2) % 3;
+      if (fits(pi, mx::kPushNone, i, mx::kPushNone) && !fits(pi, mode[pi], i, mode[i])) {
+        const int j = mode[i] != mx::kPushNone ? i : pi;  // the later projection first
+        mode[j] = mode[j] == mx::kPushFull && mode_of(plan(j, mx::kPushCompact)) == mx::kPushCompact
+                      ? mx::kPushCompact
+                      : mx::kPushNone;
+        changed = true;
+      }
+    }
+  }
 }
 
 // 2-D uint8 tensor map over a row-major [rows, k] matrix, box {128 bytes, box_rows}
@@ -158,8 +206,8 @@ struct GemmLaunch {
 int gemm_prepare(mx_handle* h, GemmLaunch* L, int M, int N, int K, const void* a,
                  const void* a_scales, const void* w, const void* w_scales, void* out, uint8_t* q,
                  uint8_t* q_scales, int q_cols, const void* x = nullptr, long ldx = 0,
-                 int groups = 1, const mx::GemmNorm* norm = nullptr) {
-  L->plan = get_plan(h, M, N, K, x != nullptr, norm != nullptr);
+                 int groups = 1, const mx::GemmNorm* norm = nullptr, int push_mode = mx::kPushFull) {
+  L->plan = get_plan(h, M, N, K, x != nullptr, norm != nullptr, push_mode);
   int rc = make_tmap(h, &L->tm_w, w, N, K, 128);
   if (rc != MX_OK) return rc;
   if (x != nullptr) {
@@ -282,10 +330,12 @@ int mx_create(mx_handle** out, int device) {
   *out = nullptr;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MX_ERR_CUDA;
-  int major = 0, minor = 0, sms = 0;
+  int major = 0, minor = 0, sms = 0, smem_sm = 0, smem_rsv = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, device) != cudaSuccess)
     return MX_ERR_CUDA;
   if (major != 10 || minor != 3) return MX_ERR_DEVICE;
   int prev = 0;
@@ -298,6 +348,8 @@ int mx_create(mx_handle** out, int device) {
   } else {
     h->device = device;
     h->sm_count = sms;
+    h->smem_per_sm = static_cast<size_t>(smem_sm);
+    h->smem_reserved = static_cast<size_t>(smem_rsv);
     h->env = mx::read_plan_env();
     const char* pe = getenv("MX_CHAIN_PERSISTENT");
     h->chain_persistent = pe != nullptr && atoi(pe) == 1;
@@ -517,15 +569,20 @@ int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, co
                         debug_out1, debug_out2, s);
   if (rc != MX_ERR_UNSUPPORTED) return rc;
   // three launches, every tensor map encoded before the first
+  int push[3];
+  chain_push(h, M, {{w[0].n, w[0].k, false, false}, {w[1].n, w[1].k, false, false}, {w[2].n, w[2].k, false, false}},
+             push);
   GemmLaunch L[3];
   rc = gemm_prepare(h, &L[0], M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, debug_out1,
-                    static_cast<uint8_t*>(a2), static_cast<uint8_t*>(a2_scales), g1_cols);
+                    static_cast<uint8_t*>(a2), static_cast<uint8_t*>(a2_scales), g1_cols, nullptr, 0, 1,
+                    nullptr, push[0]);
   if (rc == MX_OK)
     rc = gemm_prepare(h, &L[1], M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
-                      static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n);
+                      static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n, nullptr, 0, 1,
+                      nullptr, push[1]);
   if (rc == MX_OK)
     rc = gemm_prepare(h, &L[2], M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
-                      nullptr, 0);
+                      nullptr, 0, nullptr, 0, 1, nullptr, push[2]);
   for (int i = 0; i < 3 && rc == MX_OK; ++i) rc = gemm_run(h, &L[i], true, s);
   return rc;
 }
@@ -564,9 +621,14 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
   // qr in bf16, normalizes and quantizes it in its prologue (writing a2 on the
   // way) or reads a2 written by the norm kernel, and requantizes into a3; G3.
   // Every tensor map is encoded before the first launch.
+  // (four launches: the norm kernel sits between G1 and G2, so G1 and G2
+  // are not neighbours; the check then takes G2 after G1 all the same)
+  int push[3];
+  chain_push(h, M, {{w[0].n, w[0].k, false, false}, {w[1].n, w[1].k, fused, fused}, {w[2].n, w[2].k, false, false}},
+             push);
   GemmLaunch L[3];
   rc = gemm_prepare(h, &L[0], M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, out1, nullptr,
-                    nullptr, 0);
+                    nullptr, 0, nullptr, 0, 1, nullptr, push[0]);
   if (fused) {
     L[0].args.ssq_out = h->d_ssq;
     L[0].args.ssq_cols = g1_cols;
@@ -574,13 +636,14 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
   if (rc == MX_OK && fused)
     rc = gemm_prepare(h, &L[1], M, w[1].n, w[1].k, nullptr, nullptr, w[1].w, w[1].w_scales,
                       debug_out2, static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n,
-                      out1, w[0].n, 1, &norm);
+                      out1, w[0].n, 1, &norm, push[1]);
   else if (rc == MX_OK)
     rc = gemm_prepare(h, &L[1], M, w[1].n, w[1].k, a2, a2_scales, w[1].w, w[1].w_scales, debug_out2,
-                      static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n);
+                      static_cast<uint8_t*>(a3), static_cast<uint8_t*>(a3_scales), w[1].n, nullptr, 0, 1,
+                      nullptr, push[1]);
   if (rc == MX_OK)
     rc = gemm_prepare(h, &L[2], M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
-                      nullptr, 0);
+                      nullptr, 0, nullptr, 0, 1, nullptr, push[2]);
   if (rc != MX_OK) return rc;
   rc = gemm_run(h, &L[0], true, s);
   if (rc != MX_OK) return rc;

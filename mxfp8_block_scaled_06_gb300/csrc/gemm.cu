@@ -24,12 +24,15 @@
 //    (that one thread's instruction latency bounds the loop), then frees the
 //    stage with tcgen05.commit;
 //  * the four warps read the fp32 accumulator from TMEM (warp w owns lanes
-//    32w..32w+31 = weight rows), stage it in shared memory, and after a cluster
-//    barrier each (row, 32-column block) of the output is summed over the
-//    cluster's partials in rank order by one warp; the optional fused
-//    requantization (the chain's next MXFP8 activation) takes the warp's 32
-//    values as one block; a relaxed cluster barrier keeps every CTA alive until
-//    its peers have read its partials.
+//    32w..32w+31 = weight rows) and the split-K partials are summed over the
+//    cluster in rank order: up to 16 rows every CTA pushes the partials of the
+//    outputs another rank owns into that rank's shared memory (st.async,
+//    counted on the owner's mbarrier; no cluster barrier after the MMAs), above
+//    they are staged in shared memory and, after a cluster barrier, read by the
+//    owning warp from every peer; each (row, 32-column block) is summed by one
+//    warp, and the optional fused requantization (the chain's next MXFP8
+//    activation) takes its 32 values as one block; a relaxed cluster barrier
+//    keeps every CTA alive until its peers are done with its shared memory.
 // Variants: bf16 activations quantized in the prologue into resident operand
 // tiles (kFusedA), and grouped activations (weight tile t contracts the K-slice
 // of its group of a wider activation).
@@ -38,6 +41,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include <cstdio>
 
@@ -85,13 +89,35 @@ constexpr uint32_t kSfTileBytes = 512;       // one 128x4 scale tile
 // staging area for up to kRowBatch bf16 rows of the K-range. With the RMS norm
 // (norm_blocks = K/32) follow the norm weight's K-range, the staged rows'
 // per-block sums of squares and the rows' reciprocal RMS (a float per tile row).
+// Then the mbarriers, and with the push reduction the area where the peers'
+// partials arrive (apart from the ring: a slower peer's MMAs may still be
+// reading its ring when this CTA's partials reach it).
 constexpr int kRowBatch = 32;
 constexpr int kRedRows = 4;  // rows a warp reduces at once in the several-rows epilogue
+// The push reduction's unit: g rows (g = 4, or M when M < 3) of one 32-column
+// block; unit u = 4 group + block, U = 4 ceil(M / g) units, rank j owns the units
+// [j U / S, (j + 1) U / S), and each rank's slot holds ceil(U / S) units of
+// 32 lanes x g floats.
+__host__ __device__ inline int push_rows_per_unit(int M) { return M < 3 ? M : 4; }
+__host__ __device__ inline int push_units(int M) {
+  const int g = push_rows_per_unit(M);
+  return 4 * ((M + g - 1) / g);
+}
+__host__ __device__ inline uint32_t push_slot_bytes(int M, int S) {
+  return static_cast<uint32_t>((push_units(M) + S - 1) / S) * 128u * static_cast<uint32_t>(push_rows_per_unit(M));
+}
+// The receive area: one slot per rank, the CTA's own values in its own slot;
+// compact: one slot per peer, the own values over the CTA's ring (1/S less
+// shared memory, ~0.1 us slower to sum on GB300).
+__host__ __device__ inline uint32_t push_area_bytes(int M, int S, bool compact) {
+  return static_cast<uint32_t>(compact ? S - 1 : S) * push_slot_bytes(M, S);
+}
 struct Layout {
   uint32_t a_bytes, stage_bytes, ring_bytes, sfa_bytes, sfb_bytes, act, xraw, gam, ssq, inv, bars;
+  uint32_t red_bar, red, red_bytes;
   int stages, nsfb, nmax;
   __host__ __device__ Layout(int mtile, int stages_, int nmax_, bool fused = false, int xrows = 0,
-                             int norm_blocks = 0) {
+                             int norm_blocks = 0, uint32_t red_bytes_ = 0) {
     stages = stages_;
     nmax = nmax_;
     nsfb = (mtile + 127) / 128;
@@ -107,6 +133,9 @@ struct Layout {
     ssq = gam + (norm ? static_cast<uint32_t>(nmax) * 256u : 0u);
     inv = ssq + (norm ? static_cast<uint32_t>(xrows * norm_blocks) * 4u : 0u);
     bars = inv + (norm ? static_cast<uint32_t>(mtile) * 4u : 0u);
+    red_bar = bars + 8u * (2 * stages + 4) + 8u;
+    red = (bars + bar_bytes() + 127u) & ~127u;
+    red_bytes = red_bytes_;
   }
   __host__ __device__ uint32_t w_off(int s) const { return s * stage_bytes; }
   __host__ __device__ uint32_t a_off(int s) const { return s * stage_bytes + kWTileBytes; }
@@ -114,9 +143,10 @@ struct Layout {
   __host__ __device__ uint32_t sfb_off(int rt, int i) const {
     return ring_bytes + sfa_bytes + (rt * nmax + i) * kSfTileBytes;
   }
-  // full[stages], empty[stages], sfa, sfb, accum, x; then TMEM slot and abort flag
+  // full[stages], empty[stages], sfa, sfb, accum, x; then TMEM slot and abort
+  // flag; then the push reduction's receive barrier
   __host__ __device__ uint32_t bar_bytes() const { return 8u * (2 * stages + 4) + 16u; }
-  __host__ __device__ size_t total() const { return 1024 + bars + bar_bytes(); }
+  __host__ __device__ size_t total() const { return 1024 + (red_bytes ? red + red_bytes : bars + bar_bytes()); }
 };
 
 __host__ __device__ inline int tmem_sfa_col(int mtile) { return (mtile + 15) & ~15; }
@@ -127,6 +157,11 @@ __host__ __device__ inline int tmem_sfa_col(int mtile) { return (mtile + 15) & ~
 // no faster with six (N = 5120, K = 8192, M = 192: 6.5 -> 6.4 us); the peer loads
 // of up to four ranks are issued together.
 inline bool row_reduction(int M, int splits) { return splits <= 4 && M >= 8 * splits; }
+// The push reduction up to this many rows. Measured on GB300 (N = 2048, K = 5120,
+// graph-replayed with PDL): 3.83-4.03 us against 4.51-4.68 us from one to eight
+// rows, 4.51 against 5.11 at 16; from 32 rows on slower (6.5 against 5.8 us at
+// 32), the owners' incoming 16-byte stores queueing.
+constexpr int kPushMaxRows = 16;
 
 // The 64 bytes at src (shared memory) into w[0..15] in order, read as four
 // 16-byte loads that start at granule rot (0..3): threads that differ in rot
@@ -161,8 +196,8 @@ __device__ __forceinline__ void load_block64(const uint8_t* src, int rot, uint32
   }
 }
 
-// kRows: the epilogue's whole-row reduction for several rows per warp (see there).
-template <bool kRequant, bool kFusedA, bool kRows>
+// kRed: how the K-splits' partials are summed (Reduction).
+template <bool kRequant, bool kFusedA, int kRed>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                 const GemmArgs p) {
@@ -182,9 +217,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // grouped activations: this tile's group reads its own K-slice of A
   const int a_k0 = p.group_tiles > 0 ? (tile / p.group_tiles) * p.K : 0;
   const bool norm = kFusedA && p.norm.gamma != nullptr;
+  constexpr bool kPush = kRed == kReducePush || kRed == kReducePushCompact;
+  constexpr bool compact = kRed == kReducePushCompact;
+  const uint32_t slot = push_slot_bytes(p.M, S);
   const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S, kFusedA, min(p.M, kRowBatch),
-                 norm ? p.K / 32 : 0);
+                 norm ? p.K / 32 : 0, kPush ? push_area_bytes(p.M, S, compact) : 0u);
   const int nsfb = L.nsfb;
+  // Whether anything consumes the output columns of the tile's 32-column block
+  // q: a block nobody consumes (no bf16 output, outside the requantized and the
+  // summed-square columns) is not reduced.
+  auto want_q = [&](int q) {
+    return p.out != nullptr || (kRequant && tile * 128 + q * 32 < p.q_cols) ||
+           (p.ssq_out != nullptr && tile * 128 + q * 32 < p.ssq_cols);
+  };
+  // push reduction: this rank's units [own_lo, own_hi) (see push_units)
+  const int pg = push_rows_per_unit(p.M), units = push_units(p.M);
+  const int own_lo = split * units / S, own_hi = (split + 1) * units / S;
   if (threadIdx.x == 0) MX_TL(0, globaltimer());
 
   const uint32_t bars = base + L.bars;
@@ -208,6 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sfb_bar, 1);
     mbar_init(accum_bar, 1);
     mbar_init(x_bar, 1);
+    mbar_init(base + L.red_bar, 1);
+    if constexpr (kPush) {
+      // armed now with the bytes the S - 1 peers will store for this rank's
+      // wanted items (the peers start storing after the cluster barrier below)
+      uint32_t expect = 0;
+      for (int u = own_lo; u < own_hi; ++u)
+        if (want_q(u & 3)) expect += 128u * static_cast<uint32_t>(pg * (S - 1));
+      mbar_expect_tx(base + L.red_bar, expect);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w);
@@ -217,6 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // push reduction: the receive barriers of the whole cluster are initialised
+  // and armed before any peer stores to them (the wait is in the epilogue)
+  if constexpr (kPush) cluster_arrive_release();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sfa_col = tmem_sfa_col(p.mtile);
   const uint32_t sfb_col = sfa_col + 4 * stages;
@@ -568,31 +628,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   __syncwarp();
   float* const red = reinterpret_cast<float*>(base_ptr);
+  // push: the slots of the ranks (of the peers when compact: ranks below this
+  // one, then above it); this rank's own values
+  float* const push = reinterpret_cast<float*>(base_ptr + L.red);
+  float* const own = compact ? red : push + static_cast<uint32_t>(split) * (slot / 4);
   const bool ok = (*abort_flag == 0);
-  if (ok) {
-    for (int c0 = 0; c0 < p.mtile; c0 += 16) {
-      float v[16];
-      tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+  if constexpr (kPush) {
+    // Lane l of warp q holds column 32 q + l of every row: its g values of a
+    // unit go, as one store, to this rank's slot in the owner's receive area at
+    // the unit's place in the owner's range; this rank's own units are stored
+    // locally (own slot, or over the ring when compact). After a failed
+    // accumulator wait zeros are sent, so that no peer waits for bytes that
+    // never come.
+    cluster_wait_acquire();  // every peer's receive barrier is initialised and armed
+    if (want_q(warp)) {
+      int j = -1, lo = 0, hi = 0;  // the current owner and its units [lo, hi)
+      uint32_t peer = 0, peer_bar = 0;
+      auto send = [&](int u, float x0, float x1, float x2, float x3) {
+        while (u >= hi) {
+          ++j;
+          lo = hi;
+          hi = (j + 1) * units / S;
+          peer = map_shared_rank(base + L.red, j);
+          peer_bar = map_shared_rank(base + L.red_bar, j);
+        }
+        // at the owner: this rank's slot
+        const uint32_t at = static_cast<uint32_t>((u - lo) * 32 + lane) * 4u * static_cast<uint32_t>(pg);
+        const uint32_t off = static_cast<uint32_t>(compact && split > j ? split - 1 : split) * slot + at;
+        if (j == split) {
+          float* const d = own + at / 4;
+          d[0] = x0;
+          if (pg > 1) d[1] = x1;
+          if (pg > 2) {
+            d[2] = x2;
+            d[3] = x3;
+          }
+        } else if (pg == 4) {
+          st_async_v4(peer + off, x0, x1, x2, x3, peer_bar);
+        } else if (pg == 2) {
+          st_async_v2(peer + off, x0, x1, peer_bar);
+        } else {
+          st_async_b32(peer + off, __float_as_uint(x0), peer_bar);
+        }
+      };
+      for (int c0 = 0; c0 < p.M; c0 += 16) {
+        float v[16];
+        if (ok) {
+          tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+        } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + warp * 32 + lane] = v[j];
+          for (int jj = 0; jj < 16; ++jj) v[jj] = 0.f;
+        }
+        // unit of rows [c0 + e0, c0 + e0 + g): one unit per 4 rows, or the
+        // only unit when M < 3
+#pragma unroll
+        for (int e0 = 0; e0 < 16; e0 += 4) {
+          if (c0 + e0 >= p.M) break;  // warp-uniform
+          send(4 * ((c0 + e0) / 4) + warp, v[e0], v[e0 + 1], v[e0 + 2], v[e0 + 3]);
+        }
+      }
     }
+    tc_fence_before();
+    if (!mbar_wait(base + L.red_bar, 0)) fail();
+    __syncthreads();  // this rank's own values, stored by every warp, are read by any warp
+    if (threadIdx.x == 0) MX_TL(7, globaltimer());
+    // every store into this CTA has landed: its part of the exit barrier (an
+    // arrival waits for the thread's own stores to peers, by now delivered)
+    cluster_arrive_relaxed();
+  } else {
+    if (ok) {
+      for (int c0 = 0; c0 < p.mtile; c0 += 16) {
+        float v[16];
+        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + warp * 32 + lane] = v[j];
+      }
+    }
+    tc_fence_before();
+    cluster_sync();
+    if (threadIdx.x == 0) MX_TL(7, globaltimer());
   }
-  tc_fence_before();
-  cluster_sync();
-  if (threadIdx.x == 0) MX_TL(7, globaltimer());
 
   // ---------------- cluster reduction + bf16 (+ MXFP8) store
   if (ok) {
     const uint32_t red_addr = smem_u32(red);
     __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(p.out);
-    // Item = 32 columns of one row. A block nobody consumes (no bf16 output,
-    // outside the requantized and the summed-square columns) is not reduced: a peer's shared memory is
-    // read only for a value that is then used, so no read is in flight when the
-    // peers exit.
-    auto wanted = [&](int item) {
-      return item < p.M * 4 && (out != nullptr || (kRequant && tile * 128 + (item & 3) * 32 < p.q_cols) ||
-                                (p.ssq_out != nullptr && tile * 128 + (item & 3) * 32 < p.ssq_cols));
-    };
+    // Item = 32 columns of one row. An item nobody consumes is not reduced: a
+    // peer's shared memory is read only for a value that is then used, so no
+    // read is in flight when the peers exit.
+    auto wanted = [&](int item) { return item < p.M * 4 && want_q(item & 3); };
     auto item_addr = [&](int item) {
       return red_addr + static_cast<uint32_t>((item >> 2) * 128 + (item & 3) * 32 + lane) * 4u;
     };
@@ -627,11 +751,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) p.q_scales[swz_offset(m, col >> 5, p.q_cols >> 5)] = static_cast<uint8_t>(sbyte);
       }
     };
-    if (p.M <= S) {
+    if constexpr (kPush) {
+      // this rank's (unit, row) pairs dealt over the four warps: each value
+      // summed in rank order
+      // summed in rank order; the S <= 8 loads of a value are issued together
+      const int lg = pg == 4 ? 2 : pg - 1;  // log2 of g (1, 2 or 4)
+      for (int t = warp; t < ((own_hi - own_lo) << lg); t += 4) {
+        const int u = own_lo + (t >> lg), e = t & (pg - 1), m = (u >> 2) * pg + e;
+        if (m >= p.M || !want_q(u & 3)) continue;  // warp-uniform
+        const uint32_t at = ((static_cast<uint32_t>(u - own_lo) * 32u + lane) << lg) + e;
+        float v[8];
+        if constexpr (compact) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            v[r] = r >= S ? 0.f : r == split ? own[at] : push[static_cast<uint32_t>(r < split ? r : r - 1) * (slot / 4) + at];
+        } else {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) v[r] = r < S ? push[static_cast<uint32_t>(r) * (slot / 4) + at] : 0.f;
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < S) acc += v[r];
+        emit(4 * m + (u & 3), acc);
+      }
+    } else if (p.M <= S) {
       // at most one item per warp
       for (int item = split + S * warp; item < p.M * 4; item += 4 * S)
         if (wanted(item)) emit(item, cluster_sum(item_addr(item), S));
-    } else if (!kRows) {
+    } else if (kRed == kReduceItems) {
       // several items per warp: four items' peer loads in flight at once (the
       // warp is alone on its scheduler, so one item at a time would be
       // latency-bound), each still summed in rank order
@@ -753,8 +901,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) MX_TL(8, globaltimer());
   // the peers' reads of this CTA's partials have completed (their values were
-  // consumed), so ordering the exits needs no memory release
-  cluster_sync_relaxed();
+  // consumed), so ordering the exits needs no memory release; with the push
+  // reduction every CTA has arrived once all stores into it landed
+  if constexpr (kPush)
+    cluster_wait();
+  else
+    cluster_sync_relaxed();
 
   // ---------------- teardown
   if (*abort_flag != 0) {
@@ -842,11 +994,15 @@ PlanEnv read_plan_env() {
   env.splits = num("MX_SPLITS", 1, 8);  // a K-split cluster holds at most 8 CTAs
   env.stages = num("MX_STAGES", 1, 12);
   env.woa_splits = num("MX_WOA_SPLITS", 1, 8);
+  // MX_PUSH_ROWS: the push reduction up to this many rows (0: never)
+  const char* pr = getenv("MX_PUSH_ROWS");
+  env.push_rows = pr != nullptr ? std::max(0, std::min(atoi(pr), 256)) : -1;
   if (const char* e = getenv("MX_PLAN_AT")) snprintf(env.plan_at, sizeof(env.plan_at), "%s", e);
   return env;
 }
 
-GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool fused_a, bool norm) {
+GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool fused_a, bool norm,
+                   int push_mode) {
   int force_splits, force_stages;
   plan_override(env.plan_at, N, K, &force_splits, &force_stages);
   const int mtile = (M + 15) & ~15;
@@ -854,6 +1010,7 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool f
   const int nchunks = K / 128;
   const int nsfb = (mtile + 127) / 128;
   const int xrows = std::min(M, kRowBatch);
+  const int push_rows = env.push_rows >= 0 ? env.push_rows : kPushMaxRows;
   // the scale tiles of a CTA's K-range stay resident: at most 48 KB of them
   auto scale_bytes = [&](int sp) {
     return static_cast<size_t>((nchunks + sp - 1) / sp) * kSfTileBytes * (1 + nsfb);
@@ -885,7 +1042,15 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool f
       ++stages;
     pl.stages = stages;
     pl.tmem_cols = pow2_at_least(tmem_sfa_col(mtile) + 4 * stages * (1 + nsfb));
-    const Layout L(mtile, stages, per_cta, fused_a, xrows, norm ? K / 32 : 0);
+    // the push reduction (where asked for and its receive area fits)
+    const uint32_t area = push_area_bytes(M, splits, push_mode == kPushCompact);
+    const bool push = push_mode != kPushNone && M <= push_rows &&
+                      Layout(mtile, stages, per_cta, fused_a, xrows, norm ? K / 32 : 0, area).total() <=
+                          kMaxDynamicSmem;
+    pl.reduction = !push                         ? (row_reduction(M, splits) ? kReduceRows : kReduceItems)
+                   : push_mode == kPushCompact ? kReducePushCompact
+                                               : kReducePush;
+    const Layout L(mtile, stages, per_cta, fused_a, xrows, norm ? K / 32 : 0, push ? area : 0u);
     // CTAs that can share an SM must fit their TMEM together: ask for enough
     // shared memory that at most 512 / tmem_cols of them are resident.
     const int max_res = 512 / pl.tmem_cols;
@@ -919,14 +1084,23 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool f
 }
 
 cudaError_t set_gemm_attributes() {
-  const void* ks[8] = {reinterpret_cast<const void*>(&gemm_kernel<false, false, false>),
-                       reinterpret_cast<const void*>(&gemm_kernel<true, false, false>),
-                       reinterpret_cast<const void*>(&gemm_kernel<false, true, false>),
-                       reinterpret_cast<const void*>(&gemm_kernel<true, true, false>),
-                       reinterpret_cast<const void*>(&gemm_kernel<false, false, true>),
-                       reinterpret_cast<const void*>(&gemm_kernel<true, false, true>),
-                       reinterpret_cast<const void*>(&gemm_kernel<false, true, true>),
-                       reinterpret_cast<const void*>(&gemm_kernel<true, true, true>)};
+  const void* ks[16] = {
+      reinterpret_cast<const void*>(&gemm_kernel<false, false, kReduceItems>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, false, kReduceItems>),
+      reinterpret_cast<const void*>(&gemm_kernel<false, true, kReduceItems>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, true, kReduceItems>),
+      reinterpret_cast<const void*>(&gemm_kernel<false, false, kReduceRows>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, false, kReduceRows>),
+      reinterpret_cast<const void*>(&gemm_kernel<false, true, kReduceRows>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, true, kReduceRows>),
+      reinterpret_cast<const void*>(&gemm_kernel<false, false, kReducePush>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, false, kReducePush>),
+      reinterpret_cast<const void*>(&gemm_kernel<false, true, kReducePush>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, true, kReducePush>),
+      reinterpret_cast<const void*>(&gemm_kernel<false, false, kReducePushCompact>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, false, kReducePushCompact>),
+      reinterpret_cast<const void*>(&gemm_kernel<false, true, kReducePushCompact>),
+      reinterpret_cast<const void*>(&gemm_kernel<true, true, kReducePushCompact>)};
   for (const void* k : ks) {
     // clusters of up to 16 K-splits (beyond the portable 8)
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -964,15 +1138,17 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const 
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  const bool rows = row_reduction(args.M, plan.splits);
   const bool rq = args.q != nullptr, fx = args.x != nullptr;
   auto go = [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_a, args); };
-  if (rows) {
-    if (fx) return rq ? go(gemm_kernel<true, true, true>) : go(gemm_kernel<false, true, true>);
-    return rq ? go(gemm_kernel<true, false, true>) : go(gemm_kernel<false, false, true>);
-  }
-  if (fx) return rq ? go(gemm_kernel<true, true, false>) : go(gemm_kernel<false, true, false>);
-  return rq ? go(gemm_kernel<true, false, false>) : go(gemm_kernel<false, false, false>);
+  auto pick = [&](auto red) {
+    constexpr int R = decltype(red)::value;
+    if (fx) return rq ? go(gemm_kernel<true, true, R>) : go(gemm_kernel<false, true, R>);
+    return rq ? go(gemm_kernel<true, false, R>) : go(gemm_kernel<false, false, R>);
+  };
+  if (plan.reduction == kReducePush) return pick(std::integral_constant<int, kReducePush>{});
+  if (plan.reduction == kReducePushCompact) return pick(std::integral_constant<int, kReducePushCompact>{});
+  if (plan.reduction == kReduceRows) return pick(std::integral_constant<int, kReduceRows>{});
+  return pick(std::integral_constant<int, kReduceItems>{});
 }
 
 }  // namespace mx

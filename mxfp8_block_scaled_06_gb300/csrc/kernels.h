@@ -44,15 +44,27 @@ struct PlanEnv {
   int splits;
   int stages;
   int woa_splits;
+  int push_rows;  // the push reduction up to this many rows (0: the default)
   char plan_at[256];
 };
 PlanEnv read_plan_env();
+
+// How the K-splits' fp32 partials are summed (every form in rank order):
+// items = a warp sums 32-column items from the peers' shared memory; rows = a
+// warp sums whole rows with 16-byte peer loads; push = every CTA stores the
+// partials of the units another rank owns straight into that rank's shared
+// memory (st.async, counted on its mbarrier) and sums its own units locally,
+// with a receive slot per rank, or (compact) per peer.
+enum Reduction : int { kReduceItems = 0, kReduceRows = 1, kReducePush = 2, kReducePushCompact = 3 };
+// Whether a plan may take the push reduction, and with which receive area.
+enum PushMode : int { kPushNone = 0, kPushCompact = 1, kPushFull = 2 };
 
 struct GemmPlan {
   int mtile;
   int splits;
   int stages;
   int tmem_cols;
+  int reduction;  // Reduction
   size_t smem;
 };
 
@@ -110,9 +122,10 @@ constexpr int kTimelineSlots = 20;
 constexpr int kTimelineCtas = 512;
 #endif
 
-// fused_a: bf16 activations quantized in the kernel; norm: with the RMS norm.
+// fused_a: bf16 activations quantized in the kernel; norm: with the RMS norm;
+// push_mode: whether the push reduction may be chosen, and its receive area.
 GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool fused_a = false,
-                   bool norm = false);
+                   bool norm = false, int push_mode = kPushFull);
 cudaError_t set_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& args,
                         const GemmPlan& plan, bool pdl, cudaStream_t stream);

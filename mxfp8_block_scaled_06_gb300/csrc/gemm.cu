@@ -948,14 +948,18 @@ int pow2_at_least(int v) {
 // stand-alone launch (4.58 -> 4.87 us at M = 1), and one table serves both, so
 // that mx_gemm and the chain's G1 stay the same kernel (the chain equals the
 // composition of its entry points bit for bit); G1 keeps 8 splits up to 16
-// rows. wo_b keeps the counts timed as back-to-back launches. stages = 0: the
-// ring depth plan_gemm derives. Shapes not listed use the SM-count rule.
+// rows. Re-tuned with the push reduction (1 / 4 / 8 / 16 rows): only G2 at one
+// or two rows moved, from 2 to 4 splits (chain at one row 17.6 -> 17.3 us); G1
+// at 8 splits remains the fastest stand-alone (3.89 us at one row, against
+// 4.23 with 6 and 4.51 with 5). wo_b keeps the counts timed as back-to-back
+// launches. stages = 0: the ring depth plan_gemm derives. Shapes not listed use
+// the SM-count rule.
 struct SplitEntry {
   int n, k, max_m, splits, stages;
 };
 constexpr SplitEntry kSplitTable[] = {
     {2048, 5120, 16, 8, 0},   {2048, 5120, 256, 4, 0},                            // G1
-    {8192, 1536, 2, 2, 0},    {8192, 1536, 128, 4, 0},  {8192, 1536, 256, 2, 0},  // G2
+    {8192, 1536, 128, 4, 0},  {8192, 1536, 256, 2, 0},                            // G2
     {5120, 8192, 64, 6, 0},   {5120, 8192, 256, 3, 0},                            // G3
     {5120, 4096, 32, 8, 0},   {5120, 4096, 256, 6, 0},                            // wo_b
 };

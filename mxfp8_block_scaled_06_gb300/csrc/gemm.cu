@@ -951,7 +951,10 @@ int pow2_at_least(int v) {
 // rows. Re-tuned with the push reduction (1 / 4 / 8 / 16 rows): only G2 at one
 // or two rows moved, from 2 to 4 splits (chain at one row 17.6 -> 17.3 us); G1
 // at 8 splits remains the fastest stand-alone (3.89 us at one row, against
-// 4.23 with 6 and 4.51 with 5). wo_b keeps the counts timed as back-to-back
+// 4.23 with 6 and 4.51 with 5). G3 takes a ring of 4 stages from 5 to 12 rows:
+// its CTAs then fit beside G2's with the push reduction's receive areas
+// (chain at 8 rows 19.3 -> 18.4 us, at 12 rows 20.0 -> 19.5 us; at 1, 4 and 16
+// rows 0.2-0.4 us slower, so there it keeps 5). wo_b keeps the counts timed as back-to-back
 // launches. stages = 0: the ring depth plan_gemm derives. Shapes not listed use
 // the SM-count rule.
 struct SplitEntry {
@@ -960,7 +963,8 @@ struct SplitEntry {
 constexpr SplitEntry kSplitTable[] = {
     {2048, 5120, 16, 8, 0},   {2048, 5120, 256, 4, 0},                            // G1
     {8192, 1536, 128, 4, 0},  {8192, 1536, 256, 2, 0},                            // G2
-    {5120, 8192, 64, 6, 0},   {5120, 8192, 256, 3, 0},                            // G3
+    {5120, 8192, 4, 6, 0},    {5120, 8192, 12, 6, 4},   {5120, 8192, 64, 6, 0},   // G3
+    {5120, 8192, 256, 3, 0},
     {5120, 4096, 32, 8, 0},   {5120, 4096, 256, 6, 0},                            // wo_b
 };
 

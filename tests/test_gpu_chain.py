@@ -70,8 +70,12 @@ def test_chain_equals_composition_small(m):
     _composition(m, [(384, 640), (256, 256), (512, 256)], 256, seed=7)
 
 
-@pytest.mark.parametrize("m", [1, 8, 64, 129, 256])
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 12, 64, 129, 256])
 def test_chain_equals_composition_decode_shapes(m):
+    """The chain's projections take the push reduction with the full receive
+    area (1, 2, 8, 12 rows), G3 with the compact one (4 rows), and the
+    peer-read forms (64 rows and more), while the composed entry points run the
+    stand-alone plans: every output equal bit for bit."""
     _composition(m, [(2048, 5120), (8192, 1536), (5120, 8192)], 1536, seed=2)
 
 

@@ -30,6 +30,7 @@ struct PlanEntry {
   int M, N, K;
   bool fused, norm;
   int push_mode;
+  bool table_depth;
   mx::GemmPlan plan;
 };
 constexpr int kPlanCache = 64;
@@ -97,23 +98,24 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 // The GEMM plan of a problem, computed once per handle (mx_warmup computes those
 // of the registered shapes ahead of the first call).
 mx::GemmPlan get_plan(mx_handle* h, int M, int N, int K, bool fused = false, bool norm = false,
-                      int push_mode = mx::kPushFull) {
+                      int push_mode = mx::kPushFull, bool table_depth = true) {
   for (int i = 0; i < h->plan_count; ++i) {
     const PlanEntry& e = h->plans[i];
-    if (e.M == M && e.N == N && e.K == K && e.fused == fused && e.norm == norm && e.push_mode == push_mode)
+    if (e.M == M && e.N == N && e.K == K && e.fused == fused && e.norm == norm && e.push_mode == push_mode &&
+        e.table_depth == table_depth)
       return e.plan;
   }
-  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, h->env, fused, norm, push_mode);
+  const mx::GemmPlan plan = mx::plan_gemm(M, N, K, h->sm_count, h->env, fused, norm, push_mode, table_depth);
   const int slot = h->plan_count < kPlanCache ? h->plan_count++ : h->plan_next;
   if (h->plan_count == kPlanCache) h->plan_next = (slot + 1) % kPlanCache;
-  h->plans[slot] = PlanEntry{M, N, K, fused, norm, push_mode, plan};
+  h->plans[slot] = PlanEntry{M, N, K, fused, norm, push_mode, table_depth, plan};
   return plan;
 }
 
 // A chain projection's plan, for the co-residency check below.
 struct ChainShape {
   int N, K;
-  bool fused, norm;
+  bool fused, norm, table_depth;
 };
 
 // The push reduction of each projection of a three-launch chain (PushMode).
@@ -124,7 +126,9 @@ struct ChainShape {
 // too: where they do not, the later projection steps down first (full receive
 // area, then the compact one, then none).
 void chain_push(mx_handle* h, int M, const ChainShape (&c)[3], int (&mode)[3]) {
-  auto plan = [&](int i, int m) { return get_plan(h, M, c[i].N, c[i].K, c[i].fused, c[i].norm, m); };
+  auto plan = [&](int i, int m) {
+    return get_plan(h, M, c[i].N, c[i].K, c[i].fused, c[i].norm, m, c[i].table_depth);
+  };
   auto fits = [&](int pi, int pm, int i, int im) {
     const mx::GemmPlan prev = plan(pi, pm), next = plan(i, im);
     const int grid = c[pi].N / 128 * prev.splits;
@@ -206,8 +210,9 @@ struct GemmLaunch {
 int gemm_prepare(mx_handle* h, GemmLaunch* L, int M, int N, int K, const void* a,
                  const void* a_scales, const void* w, const void* w_scales, void* out, uint8_t* q,
                  uint8_t* q_scales, int q_cols, const void* x = nullptr, long ldx = 0,
-                 int groups = 1, const mx::GemmNorm* norm = nullptr, int push_mode = mx::kPushFull) {
-  L->plan = get_plan(h, M, N, K, x != nullptr, norm != nullptr, push_mode);
+                 int groups = 1, const mx::GemmNorm* norm = nullptr, int push_mode = mx::kPushFull,
+                 bool table_depth = true) {
+  L->plan = get_plan(h, M, N, K, x != nullptr, norm != nullptr, push_mode, table_depth);
   int rc = make_tmap(h, &L->tm_w, w, N, K, 128);
   if (rc != MX_OK) return rc;
   if (x != nullptr) {
@@ -570,7 +575,9 @@ int mx_gemm_chain(mx_handle* h, int M, const void* a1, const void* a1_scales, co
   if (rc != MX_ERR_UNSUPPORTED) return rc;
   // three launches, every tensor map encoded before the first
   int push[3];
-  chain_push(h, M, {{w[0].n, w[0].k, false, false}, {w[1].n, w[1].k, false, false}, {w[2].n, w[2].k, false, false}},
+  chain_push(h, M,
+             {{w[0].n, w[0].k, false, false, true}, {w[1].n, w[1].k, false, false, true},
+              {w[2].n, w[2].k, false, false, true}},
              push);
   GemmLaunch L[3];
   rc = gemm_prepare(h, &L[0], M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, debug_out1,
@@ -622,9 +629,13 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
   // way) or reads a2 written by the norm kernel, and requantizes into a3; G3.
   // Every tensor map is encoded before the first launch.
   // (four launches: the norm kernel sits between G1 and G2, so G1 and G2
-  // are not neighbours; the check then takes G2 after G1 all the same)
+  // are not neighbours; the check then takes G2 after G1 all the same). G3
+  // keeps its planned ring depth here: the split table's shallower ring for G3
+  // is measured after the plain G2 and is slower after the fused-norm one.
   int push[3];
-  chain_push(h, M, {{w[0].n, w[0].k, false, false}, {w[1].n, w[1].k, fused, fused}, {w[2].n, w[2].k, false, false}},
+  chain_push(h, M,
+             {{w[0].n, w[0].k, false, false, true}, {w[1].n, w[1].k, fused, fused, true},
+              {w[2].n, w[2].k, false, false, false}},
              push);
   GemmLaunch L[3];
   rc = gemm_prepare(h, &L[0], M, w[0].n, w[0].k, a1, a1_scales, w[0].w, w[0].w_scales, out1, nullptr,
@@ -643,7 +654,7 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
                       nullptr, push[1]);
   if (rc == MX_OK)
     rc = gemm_prepare(h, &L[2], M, w[2].n, w[2].k, a3, a3_scales, w[2].w, w[2].w_scales, out, nullptr,
-                      nullptr, 0, nullptr, 0, 1, nullptr, push[2]);
+                      nullptr, 0, nullptr, 0, 1, nullptr, push[2], false);
   if (rc != MX_OK) return rc;
   rc = gemm_run(h, &L[0], true, s);
   if (rc != MX_OK) return rc;

@@ -954,7 +954,9 @@ int pow2_at_least(int v) {
 // 4.23 with 6 and 4.51 with 5). G3 takes a ring of 4 stages from 5 to 12 rows:
 // its CTAs then fit beside G2's with the push reduction's receive areas
 // (chain at 8 rows 19.3 -> 18.4 us, at 12 rows 20.0 -> 19.5 us; at 1, 4 and 16
-// rows 0.2-0.4 us slower, so there it keeps 5). wo_b keeps the counts timed as back-to-back
+// rows 0.2-0.4 us slower, so there it keeps 5). After the fused-norm G2 the
+// shallower ring is slower (chain-norm at 8 rows 20.9 -> 22.0 us): that chain
+// asks for the planned depth. wo_b keeps the counts timed as back-to-back
 // launches. stages = 0: the ring depth plan_gemm derives. Shapes not listed use
 // the SM-count rule.
 struct SplitEntry {
@@ -1010,7 +1012,7 @@ PlanEnv read_plan_env() {
 }
 
 GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool fused_a, bool norm,
-                   int push_mode) {
+                   int push_mode, bool table_depth) {
   int force_splits, force_stages;
   plan_override(env.plan_at, N, K, &force_splits, &force_stages);
   const int mtile = (M + 15) & ~15;
@@ -1070,7 +1072,7 @@ GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool f
   // the table was measured with 152 SMs; other parts keep the SM-count rule
   const SplitEntry* te = sm_count == 152 ? table_entry(M, N, K) : nullptr;
   if (te != nullptr) splits = te->splits;
-  if (te != nullptr && force_stages == 0) force_stages = te->stages;
+  if (te != nullptr && force_stages == 0 && table_depth) force_stages = te->stages;
   splits = std::min(splits, std::min(8, nchunks));
   bool forced = false;
   if (env.splits > 0) {

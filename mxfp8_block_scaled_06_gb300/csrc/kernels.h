@@ -123,9 +123,10 @@ constexpr int kTimelineCtas = 512;
 #endif
 
 // fused_a: bf16 activations quantized in the kernel; norm: with the RMS norm;
-// push_mode: whether the push reduction may be chosen, and its receive area.
+// push_mode: whether the push reduction may be chosen, and its receive area;
+// table_depth: the ring depth of the split table's row (false: as planned).
 GemmPlan plan_gemm(int M, int N, int K, int sm_count, const PlanEnv& env, bool fused_a = false,
-                   bool norm = false, int push_mode = kPushFull);
+                   bool norm = false, int push_mode = kPushFull, bool table_depth = true);
 cudaError_t set_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_a, const GemmArgs& args,
                         const GemmPlan& plan, bool pdl, cudaStream_t stream);

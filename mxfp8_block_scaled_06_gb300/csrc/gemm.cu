@@ -47,6 +47,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "push.cuh"
 
 namespace mx {
 namespace {
@@ -94,24 +95,6 @@ constexpr uint32_t kSfTileBytes = 512;       // one 128x4 scale tile
 // reading its ring when this CTA's partials reach it).
 constexpr int kRowBatch = 32;
 constexpr int kRedRows = 4;  // rows a warp reduces at once in the several-rows epilogue
-// The push reduction's unit: g rows (g = 4, or M when M < 3) of one 32-column
-// block; unit u = 4 group + block, U = 4 ceil(M / g) units, rank j owns the units
-// [j U / S, (j + 1) U / S), and each rank's slot holds ceil(U / S) units of
-// 32 lanes x g floats.
-__host__ __device__ inline int push_rows_per_unit(int M) { return M < 3 ? M : 4; }
-__host__ __device__ inline int push_units(int M) {
-  const int g = push_rows_per_unit(M);
-  return 4 * ((M + g - 1) / g);
-}
-__host__ __device__ inline uint32_t push_slot_bytes(int M, int S) {
-  return static_cast<uint32_t>((push_units(M) + S - 1) / S) * 128u * static_cast<uint32_t>(push_rows_per_unit(M));
-}
-// The receive area: one slot per rank, the CTA's own values in its own slot;
-// compact: one slot per peer, the own values over the CTA's ring (1/S less
-// shared memory, ~0.1 us slower to sum on GB300).
-__host__ __device__ inline uint32_t push_area_bytes(int M, int S, bool compact) {
-  return static_cast<uint32_t>(compact ? S - 1 : S) * push_slot_bytes(M, S);
-}
 struct Layout {
   uint32_t a_bytes, stage_bytes, ring_bytes, sfa_bytes, sfb_bytes, act, xraw, gam, ssq, inv, bars;
   uint32_t red_bar, red, red_bytes;
@@ -157,11 +140,6 @@ __host__ __device__ inline int tmem_sfa_col(int mtile) { return (mtile + 15) & ~
 // no faster with six (N = 5120, K = 8192, M = 192: 6.5 -> 6.4 us); the peer loads
 // of up to four ranks are issued together.
 inline bool row_reduction(int M, int splits) { return splits <= 4 && M >= 8 * splits; }
-// The push reduction up to this many rows. Measured on GB300 (N = 2048, K = 5120,
-// graph-replayed with PDL): 3.83-4.03 us against 4.51-4.68 us from one to eight
-// rows, 4.51 against 5.11 at 16; from 32 rows on slower (6.5 against 5.8 us at
-// 32), the owners' incoming 16-byte stores queueing.
-constexpr int kPushMaxRows = 16;
 
 // The 64 bytes at src (shared memory) into w[0..15] in order, read as four
 // 16-byte loads that start at granule rot (0..3): threads that differ in rot
@@ -219,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool norm = kFusedA && p.norm.gamma != nullptr;
   constexpr bool kPush = kRed == kReducePush || kRed == kReducePushCompact;
   constexpr bool compact = kRed == kReducePushCompact;
-  const uint32_t slot = push_slot_bytes(p.M, S);
+  const PushGeometry pgeo(p.M, kPush ? S : 1, kPush ? split : 0);
+  const uint32_t slot = pgeo.slot;
   const Layout L(p.mtile, stages, (p.nchunks + S - 1) / S, kFusedA, min(p.M, kRowBatch),
                  norm ? p.K / 32 : 0, kPush ? push_area_bytes(p.M, S, compact) : 0u);
   const int nsfb = L.nsfb;
@@ -230,9 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     return p.out != nullptr || (kRequant && tile * 128 + q * 32 < p.q_cols) ||
            (p.ssq_out != nullptr && tile * 128 + q * 32 < p.ssq_cols);
   };
-  // push reduction: this rank's units [own_lo, own_hi) (see push_units)
-  const int pg = push_rows_per_unit(p.M), units = push_units(p.M);
-  const int own_lo = split * units / S, own_hi = (split + 1) * units / S;
   if (threadIdx.x == 0) MX_TL(0, globaltimer());
 
   const uint32_t bars = base + L.bars;
@@ -260,10 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kPush) {
       // armed now with the bytes the S - 1 peers will store for this rank's
       // wanted items (the peers start storing after the cluster barrier below)
-      uint32_t expect = 0;
-      for (int u = own_lo; u < own_hi; ++u)
-        if (want_q(u & 3)) expect += 128u * static_cast<uint32_t>(pg * (S - 1));
-      mbar_expect_tx(base + L.red_bar, expect);
+      mbar_expect_tx(base + L.red_bar, push_expect_bytes(pgeo, want_q));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -634,60 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* const own = compact ? red : push + static_cast<uint32_t>(split) * (slot / 4);
   const bool ok = (*abort_flag == 0);
   if constexpr (kPush) {
-    // Lane l of warp q holds column 32 q + l of every row: its g values of a
-    // unit go, as one store, to this rank's slot in the owner's receive area at
-    // the unit's place in the owner's range; this rank's own units are stored
-    // locally (own slot, or over the ring when compact). After a failed
-    // accumulator wait zeros are sent, so that no peer waits for bytes that
-    // never come.
+    // warp q sends column block q of every row (push.cuh); this rank's own
+    // units are stored locally (own slot, or over the ring when compact)
     cluster_wait_acquire();  // every peer's receive barrier is initialised and armed
-    if (want_q(warp)) {
-      int j = -1, lo = 0, hi = 0;  // the current owner and its units [lo, hi)
-      uint32_t peer = 0, peer_bar = 0;
-      auto send = [&](int u, float x0, float x1, float x2, float x3) {
-        while (u >= hi) {
-          ++j;
-          lo = hi;
-          hi = (j + 1) * units / S;
-          peer = map_shared_rank(base + L.red, j);
-          peer_bar = map_shared_rank(base + L.red_bar, j);
-        }
-        // at the owner: this rank's slot
-        const uint32_t at = static_cast<uint32_t>((u - lo) * 32 + lane) * 4u * static_cast<uint32_t>(pg);
-        const uint32_t off = static_cast<uint32_t>(compact && split > j ? split - 1 : split) * slot + at;
-        if (j == split) {
-          float* const d = own + at / 4;
-          d[0] = x0;
-          if (pg > 1) d[1] = x1;
-          if (pg > 2) {
-            d[2] = x2;
-            d[3] = x3;
-          }
-        } else if (pg == 4) {
-          st_async_v4(peer + off, x0, x1, x2, x3, peer_bar);
-        } else if (pg == 2) {
-          st_async_v2(peer + off, x0, x1, peer_bar);
-        } else {
-          st_async_b32(peer + off, __float_as_uint(x0), peer_bar);
-        }
-      };
-      for (int c0 = 0; c0 < p.M; c0 += 16) {
-        float v[16];
-        if (ok) {
-          tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) v[jj] = 0.f;
-        }
-        // unit of rows [c0 + e0, c0 + e0 + g): one unit per 4 rows, or the
-        // only unit when M < 3
-#pragma unroll
-        for (int e0 = 0; e0 < 16; e0 += 4) {
-          if (c0 + e0 >= p.M) break;  // warp-uniform
-          send(4 * ((c0 + e0) / 4) + warp, v[e0], v[e0 + 1], v[e0 + 2], v[e0 + 3]);
-        }
-      }
-    }
+    if (want_q(warp))
+      push_send<compact>(pgeo, tmem + (static_cast<uint32_t>(warp * 32) << 16), warp, lane, base + L.red,
+                         base + L.red_bar, own, ok);
     tc_fence_before();
     if (!mbar_wait(base + L.red_bar, 0)) fail();
     __syncthreads();  // this rank's own values, stored by every warp, are read by any warp
@@ -752,29 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     if constexpr (kPush) {
-      // this rank's (unit, row) pairs dealt over the four warps: each value
-      // summed in rank order
-      // summed in rank order; the S <= 8 loads of a value are issued together
-      const int lg = pg == 4 ? 2 : pg - 1;  // log2 of g (1, 2 or 4)
-      for (int t = warp; t < ((own_hi - own_lo) << lg); t += 4) {
-        const int u = own_lo + (t >> lg), e = t & (pg - 1), m = (u >> 2) * pg + e;
-        if (m >= p.M || !want_q(u & 3)) continue;  // warp-uniform
-        const uint32_t at = ((static_cast<uint32_t>(u - own_lo) * 32u + lane) << lg) + e;
-        float v[8];
-        if constexpr (compact) {
-#pragma unroll
-          for (int r = 0; r < 8; ++r)
-            v[r] = r >= S ? 0.f : r == split ? own[at] : push[static_cast<uint32_t>(r < split ? r : r - 1) * (slot / 4) + at];
-        } else {
-#pragma unroll
-          for (int r = 0; r < 8; ++r) v[r] = r < S ? push[static_cast<uint32_t>(r) * (slot / 4) + at] : 0.f;
-        }
-        float acc = 0.f;
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-          if (r < S) acc += v[r];
-        emit(4 * m + (u & 3), acc);
-      }
+      push_sum<compact>(pgeo, warp, kThreads / 32, lane, push, own, want_q, emit);
     } else if (p.M <= S) {
       // at most one item per warp
       for (int item = split + S * warp; item < p.M * 4; item += 4 * S)

@@ -187,6 +187,7 @@ struct WoaPlan {
   int splits;
   int stages;
   int tmem_cols;
+  bool push;  // the push split-K reduction (full receive area)
   size_t smem;
 };
 

@@ -21,14 +21,16 @@
 //     tcgen05.cp + tcgen05.mma.kind::mxf8f6f4.block_scale; weight refills come
 //     from a warp-uniform loop whose issuing lane rotates (copies issued by one
 //     thread are serviced one after another); 4. the cluster reduces the fp32
-//     partials over distributed shared memory, rounds to bf16 and requantizes
-//     each 32-column block.
+//     partials over distributed shared memory (up to 16 tokens by the push
+//     exchange of push.cuh, above by peer loads after a cluster barrier),
+//     rounds to bf16 and requantizes each 32-column block.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "push.cuh"
 
 namespace mx {
 namespace {
@@ -40,9 +42,10 @@ constexpr uint32_t kStageBytes = 16384;  // one weight box
 constexpr int kTokenBatch = 32;          // tokens whose raw x slices are staged at once
 
 struct WoaLayout {
-  uint32_t ring, act, sfb, sfa, xraw, cs, misc, total;
-  // tbmax = tokens staged per batch (min(T, kTokenBatch)), nmax = chunks per CTA
-  __host__ __device__ WoaLayout(int mtile, int stages, int nmax, int tbmax) {
+  uint32_t ring, act, sfb, sfa, xraw, cs, misc, red_bar, red, total;
+  // tbmax = tokens staged per batch (min(T, kTokenBatch)), nmax = chunks per CTA,
+  // red_bytes = the push exchange's receive area (0: none)
+  __host__ __device__ WoaLayout(int mtile, int stages, int nmax, int tbmax, uint32_t red_bytes = 0) {
     ring = 0;
     act = ring + stages * kStageBytes;                              // nmax x [mtile x 128] swizzled
     sfb = act + static_cast<uint32_t>(nmax) * mtile * 128;          // nmax x 512
@@ -50,10 +53,17 @@ struct WoaLayout {
     xraw = sfa + static_cast<uint32_t>(nmax) * kSfTileBytes;        // tbmax x nmax x 256
     cs = xraw + static_cast<uint32_t>(tbmax) * nmax * 256;          // tbmax x 64 floats
     misc = cs + static_cast<uint32_t>(tbmax) * 64 * 4;
+    // barriers: wfull[stages], empty[stages], accum, x, sfa; TMEM slot, abort
+    // flag; the receive barrier
+    red_bar = misc + 8 * (2 * stages + 3) + 8;
     total = misc + 8 * (2 * stages + 3) + 16;
+    red = (total + 127u) & ~127u;
+    if (red_bytes != 0) total = red + red_bytes;
   }
 };
 
+// kPush: the push split-K exchange (up to 16 tokens) instead of peer loads.
+template <bool kPush>
 __global__ void __launch_bounds__(kThreads, 1)
     wo_a_kernel(const __grid_constant__ CUtensorMap tm_w, const WoaArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -75,7 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = (split + 1) * nchunks / S - c_begin;
   const int nmax = (nchunks + S - 1) / S;
   const int stages = p.stages;
-  const WoaLayout L(p.mtile, stages, nmax, min(p.T, kTokenBatch));
+  const PushGeometry pgeo(p.T, kPush ? S : 1, kPush ? split : 0);
+  const uint32_t slot = pgeo.slot;
+  const WoaLayout L(p.mtile, stages, nmax, min(p.T, kTokenBatch), kPush ? push_area_bytes(p.T, S, false) : 0u);
+  auto want_all = [](int) { return true; };  // every column is requantized
 
   const uint32_t bars = base + L.misc;
   auto wfull = [&](int s) { return bars + 8u * s; };
@@ -94,6 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(accum_bar, 1);
     mbar_init(x_bar, 1);
     mbar_init(sfa_bar, 1);
+    mbar_init(base + L.red_bar, 1);
+    // armed now with the bytes the peers will store (after the cluster barrier below)
+    if constexpr (kPush) mbar_expect_tx(base + L.red_bar, push_expect_bytes(pgeo, want_all));
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w);
@@ -102,6 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // push: the receive barriers of the whole cluster are initialised and armed
+  // before any peer stores to them (the wait is in the epilogue)
+  if constexpr (kPush) cluster_arrive_release();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sfa_col = (p.mtile + 15) & ~15;
   const uint32_t sfb_col = sfa_col + 4 * stages;
@@ -345,56 +364,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   __syncwarp();
   float* const red = reinterpret_cast<float*>(bp + L.ring);
+  float* const push = reinterpret_cast<float*>(bp + L.red);
   const bool ok = (*abort_flag == 0);
-  if (ok && warp < 4) {
-    for (int c0 = 0; c0 < p.mtile; c0 += 16) {
-      float v[16];
-      tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+  if constexpr (kPush) {
+    // warps 0-3 (the accumulator's TMEM lanes) send their column blocks
+    cluster_wait_acquire();  // every peer's receive barrier is initialised and armed
+    if (warp < 4)
+      push_send<false>(pgeo, tmem + (static_cast<uint32_t>(warp * 32) << 16), warp, lane, base + L.red,
+                       base + L.red_bar, push + static_cast<uint32_t>(split) * (slot / 4), ok);
+    tc_fence_before();
+    if (!mbar_wait(base + L.red_bar, 0)) fail();
+    __syncthreads();  // this rank's own values, stored by warps 0-3, are read by any warp
+    // every store into this CTA has landed: its part of the exit barrier
+    cluster_arrive_relaxed();
+  } else {
+    if (ok && warp < 4) {
+      for (int c0 = 0; c0 < p.mtile; c0 += 16) {
+        float v[16];
+        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + warp * 32 + lane] = v[j];
+        for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + warp * 32 + lane] = v[j];
+      }
     }
+    tc_fence_before();
+    cluster_sync();
   }
-  tc_fence_before();
-  cluster_sync();
   if (ok) {
     const uint32_t red_addr = smem_u32(red);
     const int qcols = p.G * p.R;
     const int nwarps = kThreads / 32;
-    // four items' peer loads in flight at once, each summed in rank order
-    for (int i0 = split + S * warp; i0 < p.T * 4; i0 += nwarps * S * kSumBatch) {
-      uint32_t offs[kSumBatch];
-      bool use[kSumBatch];
-      float sums[kSumBatch];
-#pragma unroll
-      for (int b = 0; b < kSumBatch; ++b) {
-        const int item = i0 + b * nwarps * S;
-        use[b] = item < p.T * 4;
-        offs[b] = red_addr + static_cast<uint32_t>((item >> 2) * 128 + (item & 3) * 32 + lane) * 4u;
+    // bf16 and MXFP8 of one reduced item (32 columns of token m; warp-uniform call)
+    auto emit = [&](int item, float acc) {
+      const int m = item >> 2;
+      const int col = g * p.R + rt * 128 + (item & 3) * 32 + lane;
+      const __nv_bfloat16 hb = __float2bfloat16_rn(acc);
+      if (p.debug_z) p.debug_z[static_cast<size_t>(m) * qcols + col] = __bfloat16_as_ushort(hb);
+      const float v = __bfloat162float(hb);
+      // block amax in one reduction: non-negative floats order as their
+      // bits, and an Inf or NaN puts the maximum at or above Inf's bits
+      const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v)));
+      uint32_t sbyte, code;
+      if (amax_bits >= 0x7F800000u) {
+        sbyte = 0xFFu;
+        code = 0x7Fu;
+      } else {
+        sbyte = mx_scale_byte(__uint_as_float(amax_bits));
+        code = cvt_e4m3x2(v * mx_inv_scale(sbyte), 0.f) & 0xFFu;
       }
-      cluster_sum_batch(offs, use, S, sums);
+      p.q[static_cast<size_t>(m) * qcols + col] = static_cast<uint8_t>(code);
+      if (lane == 0) p.q_scales[swz_offset(m, col >> 5, qcols >> 5)] = static_cast<uint8_t>(sbyte);
+    };
+    if constexpr (kPush) {
+      push_sum<false>(pgeo, warp, nwarps, lane, push, push + static_cast<uint32_t>(split) * (slot / 4), want_all,
+                      emit);
+    } else {
+      // four items' peer loads in flight at once, each summed in rank order
+      for (int i0 = split + S * warp; i0 < p.T * 4; i0 += nwarps * S * kSumBatch) {
+        uint32_t offs[kSumBatch];
+        bool use[kSumBatch];
+        float sums[kSumBatch];
 #pragma unroll
-      for (int b = 0; b < kSumBatch; ++b) {
-        if (!use[b]) continue;  // warp-uniform
-        const int item = i0 + b * nwarps * S;
-        const int m = item >> 2;
-        const int col = g * p.R + rt * 128 + (item & 3) * 32 + lane;
-        const __nv_bfloat16 hb = __float2bfloat16_rn(sums[b]);
-        if (p.debug_z)
-          p.debug_z[static_cast<size_t>(m) * qcols + col] = __bfloat16_as_ushort(hb);
-        const float v = __bfloat162float(hb);
-        // block amax in one reduction: non-negative floats order as their
-        // bits, and an Inf or NaN puts the maximum at or above Inf's bits
-        const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v)));
-        uint32_t sbyte, code;
-        if (amax_bits >= 0x7F800000u) {
-          sbyte = 0xFFu;
-          code = 0x7Fu;
-        } else {
-          sbyte = mx_scale_byte(__uint_as_float(amax_bits));
-          code = cvt_e4m3x2(v * mx_inv_scale(sbyte), 0.f) & 0xFFu;
+        for (int b = 0; b < kSumBatch; ++b) {
+          const int item = i0 + b * nwarps * S;
+          use[b] = item < p.T * 4;
+          offs[b] = red_addr + static_cast<uint32_t>((item >> 2) * 128 + (item & 3) * 32 + lane) * 4u;
         }
-        p.q[static_cast<size_t>(m) * qcols + col] = static_cast<uint8_t>(code);
-        if (lane == 0) p.q_scales[swz_offset(m, col >> 5, qcols >> 5)] = static_cast<uint8_t>(sbyte);
+        cluster_sum_batch(offs, use, S, sums);
+#pragma unroll
+        for (int b = 0; b < kSumBatch; ++b)
+          if (use[b]) emit(i0 + b * nwarps * S, sums[b]);  // use[] is warp-uniform
       }
     }
     if (split == 0) {
@@ -406,8 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   // the peers' reads of this CTA's partials have completed (their values were
-  // consumed), so ordering the exits needs no memory release
-  cluster_sync_relaxed();
+  // consumed), so ordering the exits needs no memory release; with the push
+  // exchange every CTA has arrived once all stores into it landed
+  if constexpr (kPush)
+    cluster_wait();
+  else
+    cluster_sync_relaxed();
 
   if (*abort_flag != 0) {
     // wait (bounded) for the copies still in flight, so none lands after exit
@@ -450,7 +492,8 @@ WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count, const PlanEnv& env) 
     for (int stages = std::min(nmax, 4); stages >= 1; --stages) {
       // the fp32 partials [mtile][128] are staged in the weight ring
       if (static_cast<size_t>(stages) * kStageBytes < static_cast<size_t>(pl.mtile) * 512) break;
-      const WoaLayout L(pl.mtile, stages, nmax, tbmax);
+      pl.push = T <= kPushMaxRows;
+      const WoaLayout L(pl.mtile, stages, nmax, tbmax, pl.push ? push_area_bytes(T, splits, false) : 0u);
       if (static_cast<size_t>(L.total) + 1024 > 232448) continue;
       pl.splits = splits;
       pl.stages = stages;
@@ -466,10 +509,14 @@ WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count, const PlanEnv& env) 
 }
 
 cudaError_t set_wo_a_attributes() {
-  const void* k = reinterpret_cast<const void*>(&wo_a_kernel);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  for (const void* k : {reinterpret_cast<const void*>(&wo_a_kernel<false>),
+                        reinterpret_cast<const void*>(&wo_a_kernel<true>)}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_wo_a(const CUtensorMap& tm_w, const WoaArgs& args, const WoaPlan& plan,
@@ -489,7 +536,8 @@ cudaError_t launch_wo_a(const CUtensorMap& tm_w, const WoaArgs& args, const WoaP
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, wo_a_kernel, tm_w, args);
+  return plan.push ? cudaLaunchKernelEx(&cfg, wo_a_kernel<true>, tm_w, args)
+                   : cudaLaunchKernelEx(&cfg, wo_a_kernel<false>, tm_w, args);
 }
 
 }  // namespace mx

@@ -66,7 +66,8 @@ def step_bytes():
 # DRAM bytes per gemm_kernel launch from an ncu capture of the decode-projection
 # workload, keyed by the sha256 prefix of the kernel source it was taken on; a
 # changed kernel reports null until it is captured again.
-NCU_TRAFFIC = {"ef44984828dd5bdb": 10.893e6, "21856ef7ae979106": 10.907e6, "1d452fa6645ff44c": 10.902e6}
+NCU_TRAFFIC = {"ef44984828dd5bdb": 10.893e6, "21856ef7ae979106": 10.907e6, "1d452fa6645ff44c": 10.902e6,
+               "93ee1b1e31bdd36e": 10.901e6}
 
 
 def gemm_source_sha():

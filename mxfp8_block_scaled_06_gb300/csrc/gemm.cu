@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(base + L.red_bar, 1);
     if constexpr (kPush) {
       // armed now with the bytes the S - 1 peers will store for this rank's
-      // wanted items (the peers start storing after the cluster barrier below)
+      // wanted units (the peers start storing after the cluster barrier below)
       mbar_expect_tx(base + L.red_bar, push_expect_bytes(pgeo, want_q));
     }
     *abort_flag = 0;

@@ -320,6 +320,55 @@ size_t mx_warmup_bytes(const mx_weight* w, int nw, const int* rows, int nrows);
 int mx_warmup(mx_handle* h, const mx_weight* w, int nw, const int* rows, int nrows,
               void* scratch, size_t scratch_bytes, void* stream);
 
+/* ------------------------------------------------------------ plan queries
+ * Host-only (no device, no handle): the launch plans the entry points make,
+ * the mxfp8 page's fixed tactic per (shape, row range) as this library picks
+ * it, for inspection and tests. The tuning overrides of the environment
+ * (MX_SPLITS, MX_STAGES, MX_PLAN_AT, MX_PUSH_ROWS) apply as at mx_create. */
+
+/* How a plan sums the K-splits' fp32 partials (every form in rank order, so
+ * all give the same bits): peer loads of 32-column items, of whole rows, or
+ * the push exchange (each CTA stores the partials another rank owns into that
+ * rank's shared memory) with a receive slot per rank or, compact, per peer. */
+#define MX_REDUCE_ITEMS 0
+#define MX_REDUCE_ROWS 1
+#define MX_REDUCE_PUSH 2
+#define MX_REDUCE_PUSH_COMPACT 3
+/* The receive area a plan may take for the push exchange (mx_gemm: FULL). */
+#define MX_PUSH_NONE 0
+#define MX_PUSH_COMPACT 1
+#define MX_PUSH_FULL 2
+
+typedef struct mx_plan_info {
+  int splits;     /* K-splits: the CTAs of one cluster */
+  int stages;     /* weight ring depth */
+  int mtile;      /* rows padded to a multiple of 16 (the MMA's N) */
+  int tmem_cols;  /* tensor-memory columns per CTA */
+  int reduction;  /* MX_REDUCE_* */
+  size_t smem;    /* dynamic shared memory per CTA, bytes (above 232448: the
+                     shape is unsupported and the entry point rejects it) */
+} mx_plan_info;
+
+/* The plan of a [M, K] x [N, K]^T launch on a device with sm_count SMs, as
+ * mx_gemm (fused = 0) or mx_gemm_bf16 (fused = 1; norm = 1: the chain-norm's
+ * G2 with the RMS norm in its prologue) makes it, allowing the push exchange
+ * with receive area `push` (MX_PUSH_*). Returns MX_ERR_INVALID_ARG for
+ * M outside 1..256, N or K not a multiple of 128, sm_count < 1 or a null out. */
+int mx_plan_gemm(int M, int N, int K, int sm_count, int fused, int norm, int push,
+                 mx_plan_info* out);
+
+/* The push receive area (MX_PUSH_*) each of the three projections w[0..2] of
+ * mx_gemm_chain (norm = 0) or mx_gemm_chain_norm (norm = 1) takes at M rows on
+ * a device with sm_count SMs, smem_per_sm bytes of shared memory per SM and
+ * smem_reserved bytes reserved per resident block. Under PDL the next grid's
+ * CTAs start beside the previous grid's only where both fit an SM; for every
+ * pair of neighbours (G3 of the previous step before G1) that fits without the
+ * receive areas, the chosen forms fit too, the later projection stepping down
+ * first (full, compact, none). Shapes as for mx_gemm_chain; MX_ERR_INVALID_ARG
+ * otherwise. */
+int mx_plan_chain_push(int M, const mx_weight w[3], int norm, int sm_count, size_t smem_per_sm,
+                       size_t smem_reserved, int modes[3]);
+
 /* Read and clear the device status word: MX_OK, or MX_ERR_TIMEOUT if a kernel
  * gave up on a bounded wait since the last call. Synchronizes the device. */
 int mx_device_status(mx_handle* h, int* status);

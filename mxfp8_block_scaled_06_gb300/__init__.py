@@ -25,13 +25,24 @@ MX_FLAG_PDL = 1
 EXPORTS = ["mx_create", "mx_destroy", "mx_scale_bytes", "mx_quantize_rows",
            "mx_rmsnorm_quantize_rows", "mx_gemm", "mx_gemm_bf16", "mx_gemm_chain",
            "mx_gemm_chain_norm", "mx_gemm_chain_noalloc", "wo_a_grouped", "wo_a_grouped_unfused",
-           "mx_warmup_bytes", "mx_warmup", "mx_device_status", "mx_wait_selftest", "mx_status_string"]
+           "mx_warmup_bytes", "mx_warmup", "mx_plan_gemm", "mx_plan_chain_push", "mx_device_status",
+           "mx_wait_selftest", "mx_status_string"]
 
 _vp, _i, _l, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint
 
 
 class MxWeight(ctypes.Structure):
     _fields_ = [("w", _vp), ("w_scales", _vp), ("n", _i), ("k", _i)]
+
+
+# reduction forms and push receive areas of the plan queries (include/mx.h)
+MX_REDUCE_ITEMS, MX_REDUCE_ROWS, MX_REDUCE_PUSH, MX_REDUCE_PUSH_COMPACT = range(4)
+MX_PUSH_NONE, MX_PUSH_COMPACT, MX_PUSH_FULL = range(3)
+
+
+class MxPlanInfo(ctypes.Structure):
+    _fields_ = [("splits", _i), ("stages", _i), ("mtile", _i), ("tmem_cols", _i), ("reduction", _i),
+                ("smem", ctypes.c_size_t)]
 
 
 class MxError(RuntimeError):
@@ -67,6 +78,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx_gemm_chain_noalloc.argtypes = [_vp, _i, _vp, _vp, ctypes.POINTER(MxWeight), _i, _vp, _vp]
     lib.mx_warmup_bytes.argtypes = [ctypes.POINTER(MxWeight), _i, ctypes.POINTER(_i), _i]
     lib.mx_warmup_bytes.restype = ctypes.c_size_t
+    lib.mx_plan_gemm.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(MxPlanInfo)]
+    lib.mx_plan_chain_push.argtypes = [_i, ctypes.POINTER(MxWeight), _i, _i, ctypes.c_size_t, ctypes.c_size_t,
+                                       ctypes.POINTER(_i)]
     lib.mx_warmup.argtypes = [_vp, ctypes.POINTER(MxWeight), _i, ctypes.POINTER(_i), _i, _vp,
                               ctypes.c_size_t, _vp]
     lib.wo_a_grouped.argtypes = [_vp, _i, _vp, _l, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i,
@@ -519,6 +533,27 @@ def mx_warmup(h: Handle, weights, rows, stream=None) -> list:
             outs.append(buf[off:off + r * n * 2].view(torch.bfloat16).view(r, n))
             off += r256(r * n * 2)
     return outs
+
+
+def mx_plan_gemm(m: int, n: int, k: int, sm_count: int = 152, fused: bool = False, norm: bool = False,
+                 push: int = MX_PUSH_FULL) -> dict:
+    """The launch plan mx_gemm (fused: mx_gemm_bf16; norm: the chain-norm's
+    G2) makes for [m, k] x [n, k]^T on a device with sm_count SMs. Host only."""
+    info = MxPlanInfo()
+    _check(load_library().mx_plan_gemm(m, n, k, sm_count, int(fused), int(norm), push, ctypes.byref(info)),
+           "mx_plan_gemm")
+    return {f: getattr(info, f) for f, _ in MxPlanInfo._fields_}
+
+
+def mx_plan_chain_push(m: int, shapes, norm: bool = False, sm_count: int = 152, smem_per_sm: int = 233472,
+                       smem_reserved: int = 1024) -> list:
+    """The push receive area (MX_PUSH_*) of each projection of mx_gemm_chain
+    (norm: mx_gemm_chain_norm) at m rows; shapes = [(n, k)] * 3. Host only."""
+    ws = (MxWeight * 3)(*[MxWeight(None, None, n, k) for n, k in shapes])
+    modes = (_i * 3)()
+    _check(load_library().mx_plan_chain_push(m, ws, int(norm), sm_count, smem_per_sm, smem_reserved, modes),
+           "mx_plan_chain_push")
+    return list(modes)
 
 
 def mx_device_status(h: Handle) -> int:

@@ -124,16 +124,15 @@ struct ChainShape {
 // TMEM). For every pair of neighbours (G3 of the previous step before G1) that
 // fits without the push reduction's receive areas, the chosen forms must fit
 // too: where they do not, the later projection steps down first (full receive
-// area, then the compact one, then none).
-void chain_push(mx_handle* h, int M, const ChainShape (&c)[3], int (&mode)[3]) {
-  auto plan = [&](int i, int m) {
-    return get_plan(h, M, c[i].N, c[i].K, c[i].fused, c[i].norm, m, c[i].table_depth);
-  };
+// area, then the compact one, then none). plan(i, mode) is projection i's plan.
+template <typename PlanFn>
+void chain_push_modes(const ChainShape (&c)[3], int sm_count, size_t smem_per_sm, size_t smem_reserved,
+                      PlanFn plan, int (&mode)[3]) {
   auto fits = [&](int pi, int pm, int i, int im) {
     const mx::GemmPlan prev = plan(pi, pm), next = plan(i, im);
     const int grid = c[pi].N / 128 * prev.splits;
-    const size_t k = static_cast<size_t>((grid + h->sm_count - 1) / h->sm_count);
-    return k * (prev.smem + h->smem_reserved) + next.smem + h->smem_reserved <= h->smem_per_sm &&
+    const size_t k = static_cast<size_t>((grid + sm_count - 1) / sm_count);
+    return k * (prev.smem + smem_reserved) + next.smem + smem_reserved <= smem_per_sm &&
            k * prev.tmem_cols + next.tmem_cols <= 512;
   };
   auto mode_of = [](const mx::GemmPlan& pl) {
@@ -155,6 +154,21 @@ void chain_push(mx_handle* h, int M, const ChainShape (&c)[3], int (&mode)[3]) {
       }
     }
   }
+}
+
+void chain_push(mx_handle* h, int M, const ChainShape (&c)[3], int (&mode)[3]) {
+  chain_push_modes(
+      c, h->sm_count, h->smem_per_sm, h->smem_reserved,
+      [&](int i, int m) { return get_plan(h, M, c[i].N, c[i].K, c[i].fused, c[i].norm, m, c[i].table_depth); },
+      mode);
+}
+
+// mx_gemm_chain_norm applies the norm in G2's prologue (three launches) when
+// the rows' block sums of squares fit the handle's buffer and the fused plan fits
+// shared memory; otherwise the norm kernel runs between G1 and G2.
+bool chain_norm_fused(int M, int g1_cols, size_t fused_g2_smem) {
+  return M <= kNormFusedMaxRows && static_cast<size_t>(M) * (g1_cols / 32) * sizeof(float) <= kSsqBytes &&
+         fused_g2_smem <= mx::kMaxDynamicSmem;
 }
 
 // 2-D uint8 tensor map over a row-major [rows, k] matrix, box {128 bytes, box_rows}
@@ -617,9 +631,7 @@ int mx_gemm_chain_norm(mx_handle* h, int M, const void* a1, const void* a1_scale
   // Up to kNormFusedMaxRows rows G2 applies the norm in its prologue (three
   // launches); beyond, every one of G2's CTAs would repeat the RMS pass over all
   // rows, and the stand-alone norm kernel between G1 and G2 is faster.
-  const bool fused = M <= kNormFusedMaxRows &&
-                     static_cast<size_t>(M) * (g1_cols / 32) * sizeof(float) <= kSsqBytes &&
-                     get_plan(h, M, w[1].n, w[1].k, true, true).smem <= mx::kMaxDynamicSmem;
+  const bool fused = chain_norm_fused(M, g1_cols, get_plan(h, M, w[1].n, w[1].k, true, true).smem);
   const mx::GemmNorm norm{static_cast<const uint16_t*>(norm_weight), eps, h->d_ssq,
                           static_cast<uint16_t*>(debug_y), static_cast<uint8_t*>(a2),
                           static_cast<uint8_t*>(a2_scales)};
@@ -825,6 +837,44 @@ int mx_gemm_chain_noalloc(mx_handle* h, int M, const void* a1, const void* a1_sc
   if (rc != MX_OK) return rc;
   return mx_gemm_chain(h, M, a1, a1_scales, w, g1_cols, p, p + a2, p + a2 + s2, p + a2 + s2 + a3,
                        out, nullptr, nullptr, stream);
+}
+
+static_assert(MX_REDUCE_ITEMS == mx::kReduceItems && MX_REDUCE_ROWS == mx::kReduceRows &&
+                  MX_REDUCE_PUSH == mx::kReducePush && MX_REDUCE_PUSH_COMPACT == mx::kReducePushCompact,
+              "mx.h reduction codes");
+static_assert(MX_PUSH_NONE == mx::kPushNone && MX_PUSH_COMPACT == mx::kPushCompact && MX_PUSH_FULL == mx::kPushFull,
+              "mx.h push codes");
+
+int mx_plan_gemm(int M, int N, int K, int sm_count, int fused, int norm, int push, mx_plan_info* out) {
+  if (out == nullptr || M < 1 || M > 256 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0 ||
+      sm_count < 1 || push < MX_PUSH_NONE || push > MX_PUSH_FULL || (norm && !fused))
+    return MX_ERR_INVALID_ARG;
+  const mx::GemmPlan pl = mx::plan_gemm(M, N, K, sm_count, mx::read_plan_env(), fused != 0, norm != 0, push);
+  *out = mx_plan_info{pl.splits, pl.stages, pl.mtile, pl.tmem_cols, pl.reduction, pl.smem};
+  return MX_OK;
+}
+
+int mx_plan_chain_push(int M, const mx_weight w[3], int norm, int sm_count, size_t smem_per_sm,
+                       size_t smem_reserved, int modes[3]) {
+  if (w == nullptr || modes == nullptr || M < 1 || M > 256 || sm_count < 1) return MX_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (w[i].n < 128 || w[i].n % 128 != 0 || w[i].k < 128 || w[i].k % 128 != 0) return MX_ERR_INVALID_ARG;
+  if (w[1].k > w[0].n || w[2].k != w[1].n) return MX_ERR_INVALID_ARG;
+  const mx::PlanEnv env = mx::read_plan_env();
+  const bool fused =
+      norm != 0 && chain_norm_fused(M, w[1].k, mx::plan_gemm(M, w[1].n, w[1].k, sm_count, env, true, true).smem);
+  const ChainShape c[3] = {{w[0].n, w[0].k, false, false, true},
+                           {w[1].n, w[1].k, fused, fused, true},
+                           {w[2].n, w[2].k, false, false, norm == 0}};
+  int m[3];
+  chain_push_modes(
+      c, sm_count, smem_per_sm, smem_reserved,
+      [&](int i, int pm) {
+        return mx::plan_gemm(M, c[i].N, c[i].K, sm_count, env, c[i].fused, c[i].norm, pm, c[i].table_depth);
+      },
+      m);
+  for (int i = 0; i < 3; ++i) modes[i] = m[i];
+  return MX_OK;
 }
 
 int mx_device_status(mx_handle* h, int* status) {

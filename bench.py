@@ -780,6 +780,29 @@ def run_timeline(args):
             h, q1[0], q1[1], cw[i % cset], nw, 1e-6, g1_cols=CHAIN_G1_COLS, out1=out1, stream=stream,
             **bufs), 4, period=3,
             names=("G1", "G2+norm", "G3") if m <= 16 else ("G1", "G2 (after the norm kernel)", "G3"))
+    # WO-A (fused, with the push exchange up to 16 tokens), alone and followed by wo_b
+    G, H, R, D = WOA["G"], WOA["H"], WOA["R"], WOA["D"]
+    pair = [(G * R, H * D), WOB]
+    wset = rig.copies(sum(w_bytes(n, k) for n, k in pair))
+    ww = rig.weight_set(pair, seed=3, ncopies=wset)
+    cs = torch.from_numpy(synth.rope_cos_sin_cache(65536)).to(rig.dev)
+    for t in (1, 8):
+        x = torch.from_numpy(synth.normal_bf16(3 + t, synth.TAG_X, (t, G * H, D)).view(np.int16)).view(
+            torch.bfloat16).to(rig.dev)
+        pos = torch.from_numpy(synth.positions(3 + t, synth.TAG_POS, t)).to(rig.dev)
+        q = torch.empty((t, G * R), dtype=torch.uint8, device=rig.dev)
+        qs = torch.empty(mx.mx_scale_bytes(t, G * R), dtype=torch.uint8, device=rig.dev)
+        ob = torch.empty((t, WOB[0]), dtype=torch.bfloat16, device=rig.dev)
+
+        def woa(i, x=x, pos=pos, q=q, qs=qs):
+            mx.wo_a_grouped(h, x, pos, cs, *ww[i % wset][0], G, H, R, q=q, q_scales=qs, early_trigger=True,
+                            stream=stream)
+
+        def woa_wob(i, q=q, qs=qs, ob=ob):
+            woa(i)
+            mx.mx_gemm(h, q, qs, *ww[i % wset][1], out=ob, pdl=True, stream=stream)
+        out[f"wo_a_T{t}"] = record(woa, 12)
+        out[f"wo_a_wo_b_T{t}"] = record(woa_wob, 6, period=2, names=("WO-A", "wo_b"))
     for n, k in SWEEP_SHAPES:
         ws = rig.weight_set([(n, k)], seed=4, ncopies=rig.copies(w_bytes(n, k)))
         for m in (32, 64, 128, 192, 256):

@@ -763,6 +763,11 @@ int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* po
   args.debug_xs = static_cast<uint8_t*>(debug_xs);
   args.early_trigger = early_trigger;
   args.status = h->d_status;
+#ifdef MX_TIMELINE
+  args.tl = nullptr;
+  if (h->d_tl != nullptr && G * (R / 128) * plan.splits <= mx::kTimelineCtas && h->tl_next < kTimelineLaunches)
+    args.tl = h->d_tl + static_cast<size_t>(h->tl_next++) * mx::kTimelineCtas * mx::kTimelineSlots;
+#endif
   return cuda_status(mx::launch_wo_a(tm_w, args, plan, static_cast<cudaStream_t>(stream)));
 }
 

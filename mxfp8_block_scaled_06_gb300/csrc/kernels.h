@@ -207,6 +207,9 @@ struct WoaArgs {
   uint8_t* debug_xs;
   int early_trigger;
   int* status;
+#ifdef MX_TIMELINE
+  unsigned long long* tl;  // kTimelineSlots %globaltimer stamps per CTA, or null
+#endif
 };
 
 WoaPlan plan_wo_a(int T, int G, int H, int R, int sm_count, const PlanEnv& env);

@@ -41,6 +41,24 @@ constexpr uint32_t kSfTileBytes = 512;
 constexpr uint32_t kStageBytes = 16384;  // one weight box
 constexpr int kTokenBatch = 32;          // tokens whose raw x slices are staged at once
 
+// Timeline build (-DMX_TIMELINE): %globaltimer stamps of one CTA's phases in
+// p.tl, in the GEMM's slot numbering: 0 entry, 4 grid-dependency wait returned,
+// 5 first chunk landed, 6 accumulator complete, 7 partials exchanged (push:
+// received; else the cluster barrier), 8 reduction done, 9 exit, 10 SM id,
+// 12 activation quantized, 14 first token batch of x landed, 15 last chunk
+// landed, 16 every MMA issued.
+#ifdef MX_TIMELINE
+#define MX_TL(slot, v)                                                             \
+  do {                                                                             \
+    if (p.tl != nullptr)                                                           \
+      p.tl[(blockIdx.y * gridDim.x + blockIdx.x) * kTimelineSlots + (slot)] = (v); \
+  } while (0)
+#else
+#define MX_TL(slot, v) \
+  do {                 \
+  } while (0)
+#endif
+
 struct WoaLayout {
   uint32_t ring, act, sfb, sfa, xraw, cs, misc, red_bar, red, total;
   // tbmax = tokens staged per batch (min(T, kTokenBatch)), nmax = chunks per CTA,
@@ -70,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* const bp = smem_raw + (base - raw_addr);
+  if (threadIdx.x == 0) MX_TL(0, globaltimer());
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -152,6 +171,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   int x_batches = 0;
   if (!p.early_trigger) pdl_launch_dependents();
   pdl_wait();
+  if (threadIdx.x == 0) MX_TL(4, globaltimer());
+#ifdef MX_TIMELINE
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    MX_TL(10, static_cast<unsigned long long>(smid));
+  }
+#endif
 
   // ---------------- prologue: RoPE + MX quantize into the swizzled operand
   const uint32_t act_tile_bytes = static_cast<uint32_t>(p.mtile) * 128u;
@@ -195,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cs[idx] = p.cos_sin[static_cast<size_t>(pos) * 64 + (idx & 63)];
     }
     if (!mbar_wait(x_bar, batch & 1)) fail();
+    if (batch == 0 && threadIdx.x == 0) MX_TL(14, globaltimer());
     __syncthreads();
     const int total = tb * units_per_token;
     for (int b0 = 0; b0 < total; b0 += kThreads) {
@@ -272,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   fence_proxy_async_smem();
   __syncthreads();
+  if (threadIdx.x == 0) MX_TL(12, globaltimer());
 
   if (warp == 0) {
     // ---------------- weight ring refills (warp-uniform, rotating issuing lane):
@@ -323,6 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) fail();
           break;
         }
+        if (i == 0 && lane == 0) MX_TL(5, globaltimer());
+        if (i == n - 1 && lane == 0) MX_TL(15, globaltimer());
         tc_fence_after();
         if (elect_one()) {
           tmem_cp_32x128b_x4_lh(ta, f_lo, sf_hi);
@@ -356,11 +387,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (elect_one()) tc_commit(accum_bar);
     __syncwarp();
+    if (lane == 0) MX_TL(16, globaltimer());
   }
   __syncwarp();
 
   // ---------------- epilogue
   if (!mbar_wait(accum_bar, 0)) fail();
+  if (threadIdx.x == 0) MX_TL(6, globaltimer());
   tc_fence_after();
   __syncwarp();
   float* const red = reinterpret_cast<float*>(bp + L.ring);
@@ -375,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     if (!mbar_wait(base + L.red_bar, 0)) fail();
     __syncthreads();  // this rank's own values, stored by warps 0-3, are read by any warp
+    if (threadIdx.x == 0) MX_TL(7, globaltimer());
     // every store into this CTA has landed: its part of the exit barrier
     cluster_arrive_relaxed();
   } else {
@@ -388,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     cluster_sync();
+    if (threadIdx.x == 0) MX_TL(7, globaltimer());
   }
   if (ok) {
     const uint32_t red_addr = smem_u32(red);
@@ -443,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (threadIdx.x == 0) MX_TL(8, globaltimer());
   // the peers' reads of this CTA's partials have completed (their values were
   // consumed), so ordering the exits needs no memory release; with the push
   // exchange every CTA has arrived once all stores into it landed
@@ -462,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
+  if (threadIdx.x == 0) MX_TL(9, globaltimer());
 }
 
 int pow2_at_least(int v) {

@@ -169,6 +169,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               static_cast<uint32_t>(n) * kSfTileBytes, sfa_bar, pol_w);
   }
   int x_batches = 0;
+  // shared memory only, so before the wait: zero the padding rows [T, mtile) of
+  // every chunk tile and all scale tiles (the quantized rows are written over
+  // them after the first batch's barrier below)
+  const uint32_t act_tile_bytes = static_cast<uint32_t>(p.mtile) * 128u;
+  {
+    const int pad_rows = p.mtile - p.T;
+    for (int idx = threadIdx.x; idx < n * pad_rows * 8; idx += kThreads) {
+      const int i = idx / (pad_rows * 8);
+      const int rem = idx % (pad_rows * 8);
+      const int m = p.T + rem / 8;
+      *reinterpret_cast<uint4*>(bp + L.act + i * act_tile_bytes + m * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    for (int idx = threadIdx.x; idx < n * 32; idx += kThreads)
+      *reinterpret_cast<uint4*>(bp + L.sfb + idx * 16) = make_uint4(0, 0, 0, 0);
+  }
   if (!p.early_trigger) pdl_launch_dependents();
   pdl_wait();
   if (threadIdx.x == 0) MX_TL(4, globaltimer());
@@ -181,20 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 
   // ---------------- prologue: RoPE + MX quantize into the swizzled operand
-  const uint32_t act_tile_bytes = static_cast<uint32_t>(p.mtile) * 128u;
-  {
-    // zero the padding rows [T, mtile) of every chunk tile and all scale tiles
-    const int pad_rows = p.mtile - p.T;
-    for (int idx = threadIdx.x; idx < n * pad_rows * 8; idx += kThreads) {
-      const int i = idx / (pad_rows * 8);
-      const int rem = idx % (pad_rows * 8);
-      const int m = p.T + rem / 8;
-      *reinterpret_cast<uint4*>(bp + L.act + i * act_tile_bytes + m * 128 + (rem % 8) * 16) =
-          make_uint4(0, 0, 0, 0);
-    }
-    for (int idx = threadIdx.x; idx < n * 32; idx += kThreads)
-      *reinterpret_cast<uint4*>(bp + L.sfb + idx * 16) = make_uint4(0, 0, 0, 0);
-  }
   const size_t xq_stride = static_cast<size_t>(p.G) * kg;
   const int units_per_token = n * 16;  // 8-element units in the CTA's K-slice
   for (int t0 = 0, batch = 0; t0 < p.T; t0 += kTokenBatch, ++batch) {

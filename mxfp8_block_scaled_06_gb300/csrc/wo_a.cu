@@ -45,8 +45,9 @@ constexpr int kTokenBatch = 32;          // tokens whose raw x slices are staged
 // p.tl, in the GEMM's slot numbering: 0 entry, 4 grid-dependency wait returned,
 // 5 first chunk landed, 6 accumulator complete, 7 partials exchanged (push:
 // received; else the cluster barrier), 8 reduction done, 9 exit, 10 SM id,
-// 12 activation quantized, 14 first token batch of x landed, 15 last chunk
-// landed, 16 every MMA issued.
+// 12 activation quantized, 13 the first batch's barrier passed, 14 first token
+// batch of x landed, 15 last chunk landed, 16 every MMA issued, 17 thread 0's
+// units of the first batch quantized.
 #ifdef MX_TIMELINE
 #define MX_TL(slot, v)                                                             \
   do {                                                                             \
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- prologue: RoPE + MX quantize into the swizzled operand
   const size_t xq_stride = static_cast<size_t>(p.G) * kg;
   const int units_per_token = n * 16;  // 8-element units in the CTA's K-slice
+  const float inv_units = 1.f / static_cast<float>(units_per_token);
   for (int t0 = 0, batch = 0; t0 < p.T; t0 += kTokenBatch, ++batch) {
     const int tb = min(kTokenBatch, p.T - t0);
     if (warp == 0) {
@@ -226,16 +228,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(x_bar, batch & 1)) fail();
     if (batch == 0 && threadIdx.x == 0) MX_TL(14, globaltimer());
     __syncthreads();
+    if (batch == 0 && threadIdx.x == 0) MX_TL(13, globaltimer());
     const int total = tb * units_per_token;
     for (int b0 = 0; b0 < total; b0 += kThreads) {
       const int u = b0 + threadIdx.x;
       const bool valid = u < total && *abort_flag == 0;
-      const int ml = u / units_per_token;       // token within the batch
-      const int ul = u % units_per_token;       // 8-element unit within the slice
+      // token within the batch and 8-element unit within the slice: u split by
+      // units_per_token through a float reciprocal, corrected to the exact
+      // integer quotient (u < 32 tokens x 512 units: the estimate is off by at
+      // most one)
+      int ml = __float2int_rz(__int2float_rn(u) * inv_units);
+      if ((ml + 1) * units_per_token <= u) ++ml;
+      if (ml * units_per_token > u) --ml;
+      const int ul = u - ml * units_per_token;
       const int blk = ul >> 2;                  // 32-block within the slice
       const int sub = ul & 3;
       const int kin = c_begin * 128 + ul * 8;   // K index within the group
-      const int d = kin % p.D;
+      const int d = kin & (p.D - 1);            // D = 512 (448 + 64), a power of two
       float v[8];
       float amax = 0.f;
       uint32_t nonfinite = 0;
@@ -297,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (batch == 0 && threadIdx.x == 0) MX_TL(17, globaltimer());
     fence_proxy_async_smem();
     __syncthreads();  // the next batch reuses the raw slices
   }

@@ -31,23 +31,29 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   // streams its weights first) start now; wait for the previous kernel before
   // touching memory it may produce or read.
   pdl_launch_dependents();
-  pdl_wait();
+  // The warp's row and 32-block (or padding rows) touch no memory, so they are
+  // worked out before the wait: its divisions stay off the path from the
+  // previous kernel's end to the first load.
   const long gw = static_cast<long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int nblk = K >> 5;
   const int cpad4 = (nblk + 3) & ~3;
   const long real_warps = static_cast<long>(M) * groups_per_row;
-  if (gw >= real_warps) {
+  const bool pad = gw >= real_warps;
+  long wq = (pad ? gw - real_warps : gw) / groups_per_row;
+  int wgrp = static_cast<int>((pad ? gw - real_warps : gw) - wq * groups_per_row);
+  asm volatile("" : "+l"(wq), "+r"(wgrp));  // computed before the wait, not sunk below it
+  pdl_wait();
+  if (pad) {
     // padding rows [M, rows_total) of the swizzled scales: zero, kPadRows rows per warp
-    const long pw = gw - real_warps;
-    const int r0 = M + static_cast<int>(pw / groups_per_row) * kPadRows;
-    const int blk = static_cast<int>(pw % groups_per_row) * 8 + (lane >> 2);
+    const int r0 = M + static_cast<int>(wq) * kPadRows;
+    const int blk = wgrp * 8 + (lane >> 2);
     if (r0 >= rows_total || (lane & 3) != 0 || blk >= cpad4) return;
     for (int r = r0; r < min(r0 + kPadRows, rows_total); ++r) scales[swz_offset(r, blk, cpad4)] = 0;
     return;
   }
-  const int row = static_cast<int>(gw / groups_per_row);
-  const int grp = static_cast<int>(gw % groups_per_row);
+  const int row = static_cast<int>(wq);
+  const int grp = wgrp;
   const int blk = grp * 8 + (lane >> 2);
   const int sub = lane & 3;
   const bool valid = row < M && blk < nblk;

@@ -66,7 +66,10 @@ struct mx_handle {
 constexpr size_t kWoaScratchBytes = (size_t{8} << 20) + (size_t{256} << 10) + 256;
 // Measured on GB300 (4 groups x 1024 rows, 8 heads of 512): the fused kernel
 // is faster up to 8 tokens (7.5 against 8.1 us), the two launches from 12 on
-// (8.3 against 8.4 us; 19 against 75 us at 128 tokens).
+// (8.3 against 8.4 us; 19 against 75 us at 128 tokens). Re-measured with both
+// paths on the push split-K exchange: the two launches are faster from 10
+// tokens on (7.85 / 7.85 / 8.12 us against 8.04 / 8.19 / 8.96 us at 10 / 12 /
+// 16 tokens).
 constexpr int kWoaFusedMaxTokens = 8;
 // mx_gemm_chain_norm applies the RMS norm in G2's prologue up to this many rows
 // (measured on GB300 with N1 = 2048, qr 1536, N2 = 8192, N3 = 5120; beyond, G2's

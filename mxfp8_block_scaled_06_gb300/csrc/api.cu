@@ -74,6 +74,9 @@ constexpr int kWoaFusedMaxTokens = 8;
 // mx_gemm_chain_norm applies the RMS norm in G2's prologue up to this many rows
 // (measured on GB300 with N1 = 2048, qr 1536, N2 = 8192, N3 = 5120; beyond, G2's
 // CTAs each quantizing their K-range of every row cost more than a launch).
+// Re-measured with the push split-K exchange: from 9 to 16 rows the fused form
+// is still the faster (21.9 / 22.8 / 23.7 us against 25.4 / 25.0 / 25.6 us at
+// 10 / 12 / 16 rows).
 constexpr int kNormFusedMaxRows = 16;
 // the block sums of squares G1 hands to G2 there: [M, g1_cols / 32] floats
 constexpr size_t kSsqBytes = size_t{64} << 10;

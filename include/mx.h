@@ -280,9 +280,9 @@ int wo_a_grouped(mx_handle* h, int T, const void* x, long ldx, const int64_t* po
  *   z          optional [T, G*R] bf16 (the pre-quantization output), or null.
  *   other arguments as in wo_a_grouped (H is not limited to 8 here).
  * q / q_scales equal mx_quantize_rows of bf16(z). On GB300 the fused kernel is
- * faster up to 8 tokens and this path from 12 on (T = 32: 9.9 vs 15.8 us;
- * T = 128: 19.4 vs 74.7 us), so wo_a_grouped itself takes this path above 8
- * tokens. Constraints: 1 <= T <= 256,
+ * faster up to 8 tokens and this path from 10 on (T = 10: 7.85 vs 8.04 us;
+ * T = 32: 9.9 vs 15.8 us; T = 128: 19.4 vs 74.7 us), so wo_a_grouped itself
+ * takes this path above 8 tokens. Constraints: 1 <= T <= 256,
  * d_nope = 448, d_rope = 64, R % 128 == 0, else MX_ERR_UNSUPPORTED. A position
  * outside [0, max_pos) reads cache row 0 and is reported by mx_device_status,
  * as in wo_a_grouped. */

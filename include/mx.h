@@ -150,11 +150,12 @@ int mx_gemm(mx_handle* h, int M, int N, int K, const void* a, const void* a_scal
  * Constraints: as mx_gemm; MX_ERR_UNSUPPORTED also when the K-range's
  * quantized rows do not fit in one CTA's shared memory (large M with few
  * K-splits): the caller then uses mx_quantize_rows + mx_gemm.
- * Cost: every CTA quantizes the K-range it contracts (one 32-block per
- * thread), so the N/128 weight tiles repeat that work; it saves a launch, and
- * on GB300 at N = 2048, K = 5120 it is faster than mx_quantize_rows + mx_gemm
- * from one to four rows (4.65 / 4.71 / 4.84 us at 1 / 2 / 4 rows against
- * 5.12 / 5.18 / 5.28 us), slower at eight (5.57 against 5.34 us). */
+ * Cost: every CTA quantizes the K-range it contracts (each 32-block split
+ * over up to 8 threads when the rows are few), so the N/128 weight tiles
+ * repeat that work; it saves a launch, and on GB300 at N = 2048, K = 5120 it
+ * is faster than mx_quantize_rows + mx_gemm from one to four rows (4.44 /
+ * 4.46 / 4.81 us at 1 / 2 / 4 rows against 1.17 us + 3.85 / 3.89 / 4.03 us),
+ * slower at eight (5.57 against 1.17 + 4.01 us). */
 int mx_gemm_bf16(mx_handle* h, int M, int N, int K, const void* x, long ldx,
                  const void* w, const void* w_scales, void* out, unsigned flags,
                  void* stream);

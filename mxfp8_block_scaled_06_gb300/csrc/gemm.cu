@@ -300,6 +300,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) MX_TL(10, tl_smid());
   if (threadIdx.x == 0) MX_TL(11, static_cast<unsigned long long>(n));
 #endif
+  // In-kernel quantization: each 32-block of a row batch is split over tpb
+  // threads (a power of two up to 8, as many as the CTA's threads allow for the
+  // first batch, so a few rows still spread over the CTA); a thread's first
+  // (row, block) of a batch and its stride, worked out here, before the wait,
+  // where the divisions cost nothing (the empty asm keeps them here).
+  int q_tpb = 1, q_row0 = 0, q_blk0 = 0, q_drow = 0, q_dblk = 0;
+  if constexpr (kFusedA) {
+    const int bpr = n * 4;
+    const int total0 = min(p.M, kRowBatch) * bpr;
+    q_tpb = total0 * 8 <= kThreads ? 8 : total0 * 4 <= kThreads ? 4 : total0 * 2 <= kThreads ? 2 : 1;
+    const int w = static_cast<int>(threadIdx.x) / q_tpb, dw = kThreads / q_tpb;
+    q_row0 = w / bpr;
+    q_blk0 = w - q_row0 * bpr;
+    q_drow = dw / bpr;
+    q_dblk = dw - q_drow * bpr;
+    asm volatile("" : "+r"(q_tpb), "+r"(q_row0), "+r"(q_blk0), "+r"(q_drow), "+r"(q_dblk));
+  }
   if constexpr (kFusedA) {
     // shared memory only, so before the wait: zero rows [M, mtile) of every
     // activation chunk tile, and the activation scale tiles
@@ -397,33 +414,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (batch == 0 && threadIdx.x == 0) MX_TL(13, globaltimer());
       }
-      // one 32-block per thread: its 32 values, amax and codes without shuffles
+      // tpb threads per 32-block, vpt = 32 / tpb consecutive values each: the
+      // block's amax by an xor-shuffle over its aligned group of tpb lanes (a
+      // maximum, so the same bits for any split), then each thread's codes
       const int total = rb * blocks_per_row;
       const bool go = *abort_flag == 0;
-      int row = threadIdx.x / blocks_per_row, blk = threadIdx.x % blocks_per_row;
-      const int drow = kThreads / blocks_per_row, dblk = kThreads % blocks_per_row;
-      // the four 16-byte loads of a block start at a rotated one (pairs of
-      // threads), so a warp's loads spread over all banks
-      const int rot = (threadIdx.x >> 1) & 3;
-      for (int b0 = 0; go && b0 < total; b0 += kThreads) {
-        if (b0 + static_cast<int>(threadIdx.x) < total) {
-          uint32_t xw[16];
-          load_block64(base_ptr + L.xraw + row * L.nmax * 256 + blk * 64, rot, xw);
-          float v[32];
+      auto blocks = [&](auto tpb_c) {
+        constexpr int TPB = decltype(tpb_c)::value;
+        constexpr int VPT = 32 / TPB;  // values per thread
+        constexpr int WPT = VPT / 2;   // 32-bit words (bf16 pairs) per thread
+        const int sub = static_cast<int>(threadIdx.x) & (TPB - 1);
+        int row = q_row0, blk = q_blk0;
+        for (int b0 = 0; go && b0 < total; b0 += kThreads / TPB) {
+          const bool act = b0 + static_cast<int>(threadIdx.x) / TPB < total;  // uniform over the group
+          const int m = r0 + row;
+          const int kg = c_begin * 128 + blk * 32 + sub * VPT;  // the thread's first column of K
+          uint32_t xw[WPT];
+          if (act) {
+            const uint4* const src =
+                reinterpret_cast<const uint4*>(base_ptr + L.xraw + row * L.nmax * 256 + blk * 64 + sub * VPT * 2);
+            if constexpr (WPT == 16) {
+              // a whole block per thread: its four 16-byte loads start at a
+              // rotated one (pairs of threads), so a warp's loads spread over all banks
+              load_block64(reinterpret_cast<const uint8_t*>(src), (threadIdx.x >> 1) & 3, xw);
+            } else if constexpr (WPT >= 4) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+              for (int q = 0; q < WPT / 4; ++q) {
+                const uint4 t = src[q];
+                xw[4 * q] = t.x;
+                xw[4 * q + 1] = t.y;
+                xw[4 * q + 2] = t.z;
+                xw[4 * q + 3] = t.w;
+              }
+            } else {
+              const uint2 t = *reinterpret_cast<const uint2*>(src);
+              xw[0] = t.x;
+              xw[1] = t.y;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < WPT; ++e) xw[e] = 0;
+          }
+          float v[VPT];
+#pragma unroll
+          for (int e = 0; e < WPT; ++e) {
             v[2 * e] = __uint_as_float(xw[e] << 16);
             v[2 * e + 1] = __uint_as_float(xw[e] & 0xFFFF0000u);
           }
-          const int m = r0 + row;
-          const int kg = c_begin * 128 + blk * 32;  // the block's first column of K
-          if (norm) {
+          if (norm && act) {
             // y = bf16((x * inv_rms) * gamma), as the stand-alone norm kernel
             const float inv = row_inv[m];
-            uint32_t gw[16];
-            load_block64(base_ptr + L.gam + blk * 64, rot, gw);
+            uint32_t gw[WPT];
+            const uint8_t* const gsrc = base_ptr + L.gam + blk * 64 + sub * VPT * 2;
+            if constexpr (WPT == 16) {
+              load_block64(gsrc, (threadIdx.x >> 1) & 3, gw);
+            } else if constexpr (WPT >= 4) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
+              for (int q = 0; q < WPT / 4; ++q) {
+                const uint4 t = reinterpret_cast<const uint4*>(gsrc)[q];
+                gw[4 * q] = t.x;
+                gw[4 * q + 1] = t.y;
+                gw[4 * q + 2] = t.z;
+                gw[4 * q + 3] = t.w;
+              }
+            } else {
+              const uint2 t = *reinterpret_cast<const uint2*>(gsrc);
+              gw[0] = t.x;
+              gw[1] = t.y;
+            }
+#pragma unroll
+            for (int e = 0; e < WPT; ++e) {
               const float a = __fmul_rn(__fmul_rn(v[2 * e], inv), __uint_as_float(gw[e] << 16));
               const float b = __fmul_rn(__fmul_rn(v[2 * e + 1], inv), __uint_as_float(gw[e] & 0xFFFF0000u));
               const uint32_t ha = __bfloat16_as_ushort(__float2bfloat16_rn(a));
@@ -433,54 +493,88 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[2 * e + 1] = __uint_as_float(hb << 16);
             }
             if (norm_out && p.norm.y != nullptr) {
-              uint4* const dst = reinterpret_cast<uint4*>(p.norm.y + static_cast<size_t>(m) * p.K + kg);
+              uint32_t* const dst = reinterpret_cast<uint32_t*>(p.norm.y + static_cast<size_t>(m) * p.K + kg);
+              if constexpr (WPT >= 4) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(xw[4 * q], xw[4 * q + 1], xw[4 * q + 2], xw[4 * q + 3]);
+                for (int q = 0; q < WPT / 4; ++q)
+                  reinterpret_cast<uint4*>(dst)[q] =
+                      make_uint4(xw[4 * q], xw[4 * q + 1], xw[4 * q + 2], xw[4 * q + 3]);
+              } else {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(xw[0], xw[1]);
+              }
             }
           }
           // max |v| as bits: at or above Inf's bits when any value is Inf or NaN
           uint32_t amax_bits = 0;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7FFFFFFFu);
+          for (int e = 0; e < VPT; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7FFFFFFFu);
+#pragma unroll
+          for (int o = 1; o < TPB; o <<= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o));
           uint32_t sbyte;
-          uint32_t cw[8];
+          uint32_t cw[VPT / 4];
           if (amax_bits >= 0x7F800000u) {
             sbyte = 0xFFu;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) cw[c] = 0x7F7F7F7Fu;
+            for (int c = 0; c < VPT / 4; ++c) cw[c] = 0x7F7F7F7Fu;
           } else {
             sbyte = mx_scale_byte(__uint_as_float(amax_bits));
             const float f = mx_inv_scale(sbyte);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              cw[c] = cvt_e4m3x2(v[4 * c] * f, v[4 * c + 1] * f) | (cvt_e4m3x2(v[4 * c + 2] * f, v[4 * c + 3] * f) << 16);
+            for (int c = 0; c < VPT / 4; ++c)
+              cw[c] = cvt_e4m3x2(v[4 * c] * f, v[4 * c + 1] * f) |
+                      (cvt_e4m3x2(v[4 * c + 2] * f, v[4 * c + 3] * f) << 16);
           }
-          // the block's 32 codes: two 16-byte granules of the chunk tile's
-          // 128-byte row m, swizzled by m % 8
-          const int ci = blk >> 2;
-          const int g0 = (blk & 3) * 2;
+          if (act) {
+            // the thread's VPT codes in the chunk tile's 128-byte row m, whose
+            // 16-byte granules are swizzled by m % 8: bytes [c, c + VPT) of the
+            // row, c = 32 (blk % 4) + sub VPT
+            const int ci = blk >> 2;
+            const int c = (blk & 3) * 32 + sub * VPT;
+            const uint32_t rowoff = ci * at + (m >> 3) * 1024 + (m & 7) * 128;
+            if constexpr (VPT >= 16) {
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t off = ci * at + (m >> 3) * 1024 + (m & 7) * 128 + (((g0 + hh) ^ (m & 7)) << 4);
-            *reinterpret_cast<uint4*>(base_ptr + L.act + off) =
-                make_uint4(cw[4 * hh], cw[4 * hh + 1], cw[4 * hh + 2], cw[4 * hh + 3]);
+              for (int hh = 0; hh < VPT / 16; ++hh)
+                *reinterpret_cast<uint4*>(base_ptr + L.act + rowoff + ((((c >> 4) + hh) ^ (m & 7)) << 4)) =
+                    make_uint4(cw[4 * hh], cw[4 * hh + 1], cw[4 * hh + 2], cw[4 * hh + 3]);
+            } else if constexpr (VPT == 8) {
+              *reinterpret_cast<uint2*>(base_ptr + L.act + rowoff + (((c >> 4) ^ (m & 7)) << 4) + (c & 15)) =
+                  make_uint2(cw[0], cw[1]);
+            } else {
+              *reinterpret_cast<uint32_t*>(base_ptr + L.act + rowoff + (((c >> 4) ^ (m & 7)) << 4) + (c & 15)) =
+                  cw[0];
+            }
+            if (sub == 0)
+              base_ptr[L.sfb_off(m >> 7, ci) + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (blk & 3)] =
+                  static_cast<uint8_t>(sbyte);
+            if (norm_out && p.norm.a_q != nullptr) {
+              uint8_t* const dst = p.norm.a_q + static_cast<size_t>(m) * p.K + kg;
+              if constexpr (VPT >= 16) {
+#pragma unroll
+                for (int hh = 0; hh < VPT / 16; ++hh)
+                  reinterpret_cast<uint4*>(dst)[hh] =
+                      make_uint4(cw[4 * hh], cw[4 * hh + 1], cw[4 * hh + 2], cw[4 * hh + 3]);
+              } else if constexpr (VPT == 8) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
+              } else {
+                *reinterpret_cast<uint32_t*>(dst) = cw[0];
+              }
+              if (sub == 0)
+                p.norm.a_q_scales[swz_offset(m, (kg - sub * VPT) >> 5, p.K >> 5)] = static_cast<uint8_t>(sbyte);
+            }
           }
-          base_ptr[L.sfb_off(m >> 7, ci) + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (blk & 3)] =
-              static_cast<uint8_t>(sbyte);
-          if (norm_out && p.norm.a_q != nullptr) {
-            uint4* const dst = reinterpret_cast<uint4*>(p.norm.a_q + static_cast<size_t>(m) * p.K + kg);
-            dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-            dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            p.norm.a_q_scales[swz_offset(m, kg >> 5, p.K >> 5)] = static_cast<uint8_t>(sbyte);
+          row += q_drow;
+          blk += q_dblk;
+          if (blk >= blocks_per_row) {
+            blk -= blocks_per_row;
+            ++row;
           }
         }
-        row += drow;
-        blk += dblk;
-        if (blk >= blocks_per_row) {
-          blk -= blocks_per_row;
-          ++row;
-        }
+      };
+      switch (q_tpb) {
+        case 8: blocks(std::integral_constant<int, 8>{}); break;
+        case 4: blocks(std::integral_constant<int, 4>{}); break;
+        case 2: blocks(std::integral_constant<int, 2>{}); break;
+        default: blocks(std::integral_constant<int, 1>{}); break;
       }
       __syncthreads();  // the next batch reuses the staging rows
     }

@@ -163,7 +163,9 @@ def test_chain_norm_small_shapes(m):
     _chain_norm_composition(m, [(384, 640), (256, 256), (512, 256)], 256, seed=70)
 
 
-@pytest.mark.parametrize("m", [1, 5, 16, 17, 40, 130])
+# 1, 2, 3 and 5 rows: G2 splits each 32-block of its prologue over 8, 4, 2 and
+# 2 threads (its K-range holds 12 blocks a row), from 16 rows one thread a block
+@pytest.mark.parametrize("m", [1, 2, 3, 5, 16, 17, 40, 130])
 def test_chain_norm_equals_composition_and_oracle(m):
     shapes = [(2048, 5120), (8192, 1536), (5120, 8192)]
     res, wops, ra, rsa, nw_bits = _chain_norm_composition(m, shapes, 1536, seed=60)

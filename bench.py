@@ -12,7 +12,7 @@ Python API with host buffers, SM clocks, and the CPU oracle's time on a
 bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --profile gemm|chain|wo_a|sweep   (a few plain launches for ncu)
+  python bench.py --profile gemm|bf16|chain|wo_a|sweep   (a few plain launches for ncu)
   python bench.py --timeline   (per-CTA phase timeline, timeline build of the library)
 """
 from __future__ import annotations
@@ -618,6 +618,12 @@ def run_profile(args):
             q = mx.mx_quantize_rows(h, rig.activation(m, K1, 1))
             for i in range(3):
                 mx.mx_gemm(h, q[0], q[1], *w[i % 4][0], pdl=True)
+    elif args.profile == "bf16":
+        w = rig.weight_set([(N1, K1)], 1, 4)
+        for m in (1, 8):
+            x = rig.activation(m, K1, 1)
+            for i in range(3):
+                mx.mx_gemm_bf16(h, x, *w[i % 4][0], pdl=True)
     elif args.profile == "chain":
         cw = rig.weight_set(CHAIN_SHAPES, 2, 2)
         for m in (8, 64):
@@ -933,7 +939,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMM launch from an ncu capture of the current kernel")
-    ap.add_argument("--profile", default=None, choices=["gemm", "chain", "wo_a", "sweep"])
+    ap.add_argument("--profile", default=None, choices=["gemm", "bf16", "chain", "wo_a", "sweep"])
     ap.add_argument("--timeline", action="store_true",
                     help="per-CTA phase timeline of GEMM launches (builds the -DMX_TIMELINE library)")
     ap.add_argument("--tune-chain", action="store_true",

@@ -290,7 +290,7 @@ int gemm_launch(mx_handle* h, int M, int N, int K, const void* a, const void* a_
 // The chain in one persistent kernel (chain.cu), when MX_CHAIN_PERSISTENT=1 and
 // its plan exists (up to 16 rows, K splits of each projection's GEMM plan at
 // most 8, enough resident clusters). Measured on GB300 it is slower than the
-// three launches (33 vs 19 us at one row: its weight ring fills during each
+// three launches (39.6 vs 17.1 us at one row: its weight ring fills during each
 // projection's dependency wait and every hand-off is a chain of ~0.5 us
 // latencies), so the three launches are the default.
 // Returns MX_OK after launching, MX_ERR_UNSUPPORTED when the three-launch path

@@ -43,16 +43,17 @@ def test_decode_projection_takes_push_up_to_16_rows():
 
 @pytest.mark.parametrize("n,k", [(2048, 5120), (8192, 1536), (5120, 8192), (5120, 4096), (384, 640),
                                  (256, 2048)])
-@pytest.mark.parametrize("fused", [False, True])
-def test_receive_area_is_in_the_budget(n, k, fused):
+@pytest.mark.parametrize("fused,norm", [(False, False), (True, False), (True, True)])
+def test_receive_area_is_in_the_budget(n, k, fused, norm):
     """Same ring and splits with and without push; the difference in shared
     memory is the receive area (plus under 128 bytes of alignment); a push
-    plan never exceeds the per-CTA maximum."""
+    plan never exceeds the per-CTA maximum. With the norm (the chain's G2) the
+    prologue's row sums and norm weight share the budget."""
     for m in range(1, 17):
-        none = mx.mx_plan_gemm(m, n, k, fused=fused, push=mx.MX_PUSH_NONE)
+        none = mx.mx_plan_gemm(m, n, k, fused=fused, norm=norm, push=mx.MX_PUSH_NONE)
         for push, red, compact in ((mx.MX_PUSH_FULL, mx.MX_REDUCE_PUSH, False),
                                    (mx.MX_PUSH_COMPACT, mx.MX_REDUCE_PUSH_COMPACT, True)):
-            p = mx.mx_plan_gemm(m, n, k, fused=fused, push=push)
+            p = mx.mx_plan_gemm(m, n, k, fused=fused, norm=norm, push=push)
             assert (p["splits"], p["stages"], p["tmem_cols"]) == (none["splits"], none["stages"], none["tmem_cols"])
             if p["reduction"] != red:  # push left out: it did not fit
                 assert none["smem"] + _area(m, p["splits"], compact) > MAX_SMEM or none["smem"] > MAX_SMEM

@@ -70,6 +70,13 @@ def test_bf16_tile_and_split_shapes(n, k):
     _run(6, n, k, seed=n + k)
 
 
+@pytest.mark.parametrize("m,n,k", [(3, 2048, 1408), (3, 2048, 2432)])
+def test_bf16_ragged_k_splits(m, n, k):
+    # 11 / 19 chunks over 8 K-splits: CTAs with one or two (two or three)
+    # chunks, so one launch splits its 32-blocks over 8 and 4 (4 and 2) threads
+    _run(m, n, k, seed=k)
+
+
 def test_bf16_strided_rows():
     _run(5, 512, 1024, seed=4, ldx=1024 + 40)
 
